@@ -1,0 +1,131 @@
+"""Python binding of libgbfuse.so: fused operator chains for GB300 (sm_103a).
+
+Argument marshalling only.  Every function takes torch tensors that live on
+the GPU, checks nothing the C library does not check itself, passes their
+data pointers and sizes to the C-ABI entry point of the same name (see
+include/gbfuse.h) on the current torch stream, and raises GbfError on a
+non-zero status.  There is no CPU path: importing this package fails when the
+compiled library is missing, and every call fails without a CUDA device.
+
+Build the library with `python -c "import __graft_entry__ as g; g.build()"`
+(or `python fusion_add_rmsnorm_gb300/build.py`).
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgbfuse.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run fusion_add_rmsnorm_gb300/build.py "
+                      "(this package has no CPU fallback)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+OK, EINVAL, EALIGN, EUNSUPPORTED, ELAUNCH, ETIMEOUT, EDEVICE = 0, -1, -2, -3, -4, -5, -6
+NORM_WEIGHT, NORM_NOWEIGHT, NORM_ADA = 0, 1, 2
+QKNORM_PER_HEAD, QKNORM_FULL_WIDTH = 0, 1
+ROPE_1D, ROPE_3D = 0, 1
+ACT_NONE, ACT_GELU_TANH = 0, 1
+
+_p, _i64, _i32, _f = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+
+_SIGNATURES = {
+    "gbf_add_rmsnorm_fp8": [_p, _p, _p, _p, _i32, _p, _p, _p, _p, _i64, _i64, _f, _f, _p],
+    "gbf_qkv_split_norm_rope": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _f, _i32, _p, _p, _f, _p, _p, _p,
+                                _p, _i64, _p],
+    "gbf_linear_bias_gelu": [_p, _p, _p, _p, _i64, _i64, _i64, _i32, _p],
+    "gbf_bn_fold": [_p, _p, _p, _p, _p, _p, _f, _i64, _i64, _p, _p, _p],
+    "gbf_copy": [_p, _p, _i64, _p],
+    "gbf_device_status": [_p],
+    "gbf_last_error": [],
+    "gbf_version": [],
+}
+for _name, _args in _SIGNATURES.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = ctypes.c_char_p if _name == "gbf_last_error" else ctypes.c_int
+
+EXPORTED = tuple(_SIGNATURES)
+
+
+class GbfError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"status {status}: {message}")
+        self.status = status
+
+
+def _check(status):
+    if status != OK:
+        raise GbfError(status, _lib.gbf_last_error().decode())
+    return status
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def version():
+    return _lib.gbf_version()
+
+
+def raw():
+    """The ctypes handle of libgbfuse.so, for callers that pass raw pointers."""
+    return _lib
+
+
+def add_rmsnorm_fp8(x, res_in, res_out, q_out, mode, weight=None, gate=None, ada_scale=None, ada_shift=None,
+                    eps=1e-6, fp8_scale=0.05, stream=None):
+    """gbf_add_rmsnorm_fp8 on [rows, hidden] bf16 tensors; q_out is uint8."""
+    rows, hidden = x.shape[0], x.shape[-1]
+    return _check(_lib.gbf_add_rmsnorm_fp8(_ptr(x), _ptr(res_in), _ptr(res_out), _ptr(gate), mode, _ptr(weight),
+                                           _ptr(ada_scale), _ptr(ada_shift), _ptr(q_out), rows, hidden, eps,
+                                           fp8_scale, _stream(stream)))
+
+
+def qkv_split_norm_rope(qkv, n_q_heads, n_kv_heads, head_dim, norm, q_w, k_w, eps, rope, pos, theta, q_out,
+                        k_cache, v_cache, sections=None, slots=None, cache_rows=None, stream=None):
+    """gbf_qkv_split_norm_rope; `sections` is a host sequence of three ints."""
+    tokens = qkv.shape[0]
+    sec = None if sections is None else (ctypes.c_int32 * 3)(*sections)
+    rows = k_cache.shape[0] if cache_rows is None else cache_rows
+    return _check(_lib.gbf_qkv_split_norm_rope(_ptr(qkv), tokens, n_q_heads, n_kv_heads, head_dim, norm, _ptr(q_w),
+                                               _ptr(k_w), eps, rope, _ptr(pos),
+                                               ctypes.cast(sec, ctypes.c_void_p) if sec is not None else None,
+                                               theta, _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(slots),
+                                               rows, _stream(stream)))
+
+
+def linear_bias_gelu(x, w, bias, y, act=ACT_GELU_TANH, stream=None):
+    """gbf_linear_bias_gelu: y[M, N] = act(x[M, K] @ w[N, K]^T + bias[N])."""
+    m, k = x.shape
+    n = w.shape[0]
+    return _check(_lib.gbf_linear_bias_gelu(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), m, n, k, act, _stream(stream)))
+
+
+def bn_fold(w, b, gamma, beta, mean, var, eps, w_out, b_out, stream=None):
+    """gbf_bn_fold on a weight [out_ch, ...] (flattened per output channel)."""
+    out_ch = w.shape[0]
+    inner = w.numel() // max(out_ch, 1)
+    return _check(_lib.gbf_bn_fold(_ptr(w), _ptr(b), _ptr(gamma), _ptr(beta), _ptr(mean), _ptr(var), eps, out_ch,
+                                   inner, _ptr(w_out), _ptr(b_out), _stream(stream)))
+
+
+def copy(src, dst, nbytes=None, stream=None):
+    """gbf_copy of nbytes (default: all of src) bytes."""
+    n = src.numel() * src.element_size() if nbytes is None else nbytes
+    return _check(_lib.gbf_copy(_ptr(src), _ptr(dst), n, _stream(stream)))
+
+
+def device_status(stream=None):
+    """Synchronise the stream and return (status, message) of the device error word, clearing it."""
+    s = _lib.gbf_device_status(_stream(stream))
+    return s, (_lib.gbf_last_error().decode() if s else "")

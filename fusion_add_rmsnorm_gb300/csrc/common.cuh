@@ -1,0 +1,112 @@
+// Shared device helpers for the fused kernels (sm_103a).
+//
+// Storage formats: bfloat16 activations and weights, OCP FP8 E4M3 codes,
+// float32 arithmetic in registers.  Every helper here is a thin wrapper over a
+// CUDA intrinsic; no math-library routine is re-implemented.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define GBF_DEVICE __device__ __forceinline__
+
+namespace gbf {
+
+// Bits of the device-side error word (a library-owned __device__ variable whose
+// address every launch receives; read and cleared by gbf_device_status()).
+enum : unsigned int {
+  DEV_ERR_SLOT_RANGE = 1u << 0,    // a KV-cache slot index was outside [0, cache_rows)
+  DEV_ERR_MBAR_TIMEOUT = 1u << 1,  // a bounded mbarrier wait gave up
+};
+
+GBF_DEVICE void raise_error(unsigned int* err, unsigned int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// ---------------------------------------------------------------- 16-byte I/O
+
+// Streaming 16-byte load that does not allocate in L1.  A plain (coherent)
+// load, not the read-only path: under programmatic dependent launch the data
+// may have been written by the grid this one waited for.
+GBF_DEVICE uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// 16-byte load that may be served from L1 (small broadcast vectors: weights).
+GBF_DEVICE uint4 ld_cached(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+GBF_DEVICE void st_16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+
+// ------------------------------------------------------------- bf16 packing
+
+// 8 bf16 in a uint4 -> 8 floats (exact widening).
+GBF_DEVICE void bf16x8_to_f32(uint4 v, float f[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// 2 floats -> packed bf16x2 (round to nearest even; lower address = a).
+GBF_DEVICE uint32_t f32x2_to_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+GBF_DEVICE uint4 f32x8_to_bf16x8(const float f[8]) {
+  uint4 v;
+  v.x = f32x2_to_bf16x2(f[0], f[1]);
+  v.y = f32x2_to_bf16x2(f[2], f[3]);
+  v.z = f32x2_to_bf16x2(f[4], f[5]);
+  v.w = f32x2_to_bf16x2(f[6], f[7]);
+  return v;
+}
+
+GBF_DEVICE float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+// --------------------------------------------------------------- E4M3 packing
+
+// 2 floats -> 2 E4M3 codes (round to nearest even, saturate to +-448); the
+// code of `a` lands at the lower address.
+GBF_DEVICE uint16_t f32x2_to_e4m3x2(float a, float b) {
+  return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+GBF_DEVICE uint2 f32x8_to_e4m3x8(const float f[8]) {
+  uint2 v;
+  v.x = static_cast<uint32_t>(f32x2_to_e4m3x2(f[0], f[1])) | (static_cast<uint32_t>(f32x2_to_e4m3x2(f[2], f[3])) << 16);
+  v.y = static_cast<uint32_t>(f32x2_to_e4m3x2(f[4], f[5])) | (static_cast<uint32_t>(f32x2_to_e4m3x2(f[6], f[7])) << 16);
+  return v;
+}
+
+// ------------------------------------------------------------ reductions
+
+GBF_DEVICE float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum over aligned groups of `width` lanes (width a power of two <= 32).
+GBF_DEVICE float group_sum(float v, int width) {
+  for (int o = width >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// --------------------------------------------- programmatic dependent launch
+
+// Wait until the grids this launch depends on have completed and their
+// memory is visible (a no-op when the launch carried no programmatic edge).
+GBF_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next grid in the stream to begin launching.
+GBF_DEVICE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+}  // namespace gbf

@@ -1,0 +1,107 @@
+// Internal interface between the C-ABI layer (abi.cu) and the kernel
+// translation units.  Argument structs are passed to kernels by value.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbf {
+
+enum { kNormWeight = 0, kNormNoWeight = 1, kNormAda = 2 };
+enum { kQkNormPerHead = 0, kQkNormFullWidth = 1 };
+enum { kRope1D = 0, kRope3D = 1 };
+enum { kActNone = 0, kActGeluTanh = 1 };
+
+// ------------------------------------------------------- add + RMSNorm + FP8
+struct AddRmsNormArgs {
+  const void* x;
+  const void* res_in;
+  void* res_out;
+  const void* gate;       // nullable
+  const void* weight;     // kNormWeight
+  const void* ada_scale;  // kNormAda
+  const void* ada_shift;  // kNormAda
+  void* q_out;
+  int64_t rows;
+  int64_t hidden;
+  float eps;
+  float fp8_scale;
+  int mode;
+  int tpr;                // threads per row (set by the launcher)
+  int rows_per_cta;       // (set by the launcher)
+};
+
+struct AddRmsNormPlan {
+  bool ok;
+  int nv, tpr, rows_per_cta, block;
+  int64_t grid;
+};
+
+AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden);
+cudaError_t launch_add_rmsnorm_fp8(AddRmsNormArgs a, cudaStream_t stream, bool pdl);
+
+// --------------------------------------------- packed QKV split + norm + RoPE
+constexpr int kMaxRopeSlots = 128;      // head_dim <= 256
+
+struct QkvArgs {
+  const void* qkv;
+  const void* q_w;
+  const void* k_w;
+  const int32_t* pos;
+  const int32_t* slots;   // nullable
+  void* q_out;
+  void* k_cache;
+  void* v_cache;
+  unsigned int* err;
+  int64_t tokens;
+  int64_t cache_rows;
+  int n_q, n_kv, d;
+  int norm, rope;
+  float eps;
+  int sec[3];             // 3D section widths (sum = d)
+  int n_slots;            // rotation slots per head = d / 2
+  // per slot: rotation frequency (hi + lo binary32 split of the float64 value),
+  // which grid coordinate drives it, and its (lo, hi) element pair in the head
+  float omega_hi[kMaxRopeSlots];
+  float omega_lo[kMaxRopeSlots];
+  unsigned char axis[kMaxRopeSlots];
+  unsigned char lo_idx[kMaxRopeSlots];
+  unsigned char hi_idx[kMaxRopeSlots];
+};
+
+cudaError_t launch_qkv_split_norm_rope(const QkvArgs& a, cudaStream_t stream);
+
+// ------------------------------------------------------------ BN folding
+struct BnFoldArgs {
+  const void* w;
+  const void* b;          // nullable
+  const float* gamma;
+  const float* beta;
+  const float* mean;
+  const float* var;
+  void* w_out;
+  void* b_out;
+  float eps;
+  int64_t out_ch;
+  int64_t inner;
+};
+
+cudaError_t launch_bn_fold(const BnFoldArgs& a, cudaStream_t stream);
+
+// ------------------------------------------------------------- copy probe
+cudaError_t launch_copy(const void* src, void* dst, int64_t bytes, cudaStream_t stream);
+
+// ------------------------------------------------ Linear + bias + GELU GEMM
+struct GemmArgs {
+  const void* x;          // [M, K] bf16, K-major
+  const void* w;          // [N, K] bf16, K-major
+  const void* bias;       // [N] bf16, nullable
+  void* y;                // [M, N] bf16
+  unsigned int* err;
+  int64_t m, n, k;
+  int act;
+};
+
+cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, const char** why);
+
+}  // namespace gbf

@@ -1,0 +1,143 @@
+"""Host-side tests of the C ABI: the library loads, exports every entry point
+include/gbfuse.h declares, and rejects bad arguments with the documented status
+before touching a device.  No test here launches a kernel (the pointers are
+fake addresses that the validation must never dereference)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "gbfuse.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"GBF_API\s+[\w\s\*]+?\b(gbf_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def gbf():
+    import fusion_add_rmsnorm_gb300 as g
+    return g
+
+
+def test_header_declares_the_entry_points():
+    assert declared_symbols() == sorted(["gbf_add_rmsnorm_fp8", "gbf_qkv_split_norm_rope", "gbf_linear_bias_gelu",
+                                         "gbf_bn_fold", "gbf_copy", "gbf_device_status", "gbf_last_error",
+                                         "gbf_version"])
+
+
+def test_library_exports_every_declared_symbol(gbf):
+    out = subprocess.run(["nm", "-D", "--defined-only", gbf.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (gbf_\w+)", out))
+    assert set(declared_symbols()) <= exported
+    # nothing but the documented C entry points leaks out of the library
+    assert {s for s in exported if s.startswith("gbf")} == set(declared_symbols())
+    for s in declared_symbols():
+        assert hasattr(gbf.raw(), s)
+    assert set(gbf.EXPORTED) == set(declared_symbols())
+
+
+def test_version(gbf):
+    assert gbf.version() == 10000
+
+
+F = 0x10000          # fake, 16-byte aligned "device" addresses; never dereferenced
+
+
+def A(i):
+    return ctypes.c_void_p(F * (i + 1))
+
+
+def last(gbf):
+    return gbf.raw().gbf_last_error().decode()
+
+
+def test_add_rmsnorm_validation(gbf):
+    L = gbf.raw()
+    call = lambda **k: L.gbf_add_rmsnorm_fp8(*[k.get(n, d) for n, d in [           # noqa: E731
+        ("x", A(0)), ("res_in", A(1)), ("res_out", A(2)), ("gate", None), ("mode", 0), ("weight", A(3)),
+        ("scale", None), ("shift", None), ("q", A(4)), ("rows", 4), ("hidden", 64), ("eps", 1e-6),
+        ("s", 0.05), ("stream", None)]])
+    assert call(rows=0) == gbf.OK                         # empty: nothing enqueued
+    assert call(hidden=60) == gbf.EALIGN and "multiple of 8" in last(gbf)
+    assert call(hidden=65536) == gbf.EUNSUPPORTED
+    assert call(hidden=0) == gbf.EINVAL
+    assert call(rows=-1) == gbf.EINVAL
+    assert call(mode=7) == gbf.EINVAL
+    assert call(x=None) == gbf.EINVAL
+    assert call(weight=None) == gbf.EINVAL                # WEIGHT mode needs a weight
+    assert call(mode=2) == gbf.EINVAL                     # ADA needs scale and shift
+    assert call(eps=-1.0) == gbf.EINVAL
+    assert call(s=0.0) == gbf.EINVAL
+    assert call(s=float("inf")) == gbf.EINVAL
+    assert call(eps=float("nan")) == gbf.EINVAL
+    assert call(x=ctypes.c_void_p(F + 8)) == gbf.EALIGN
+    # res_out may alias res_in exactly, but not overlap x or partially overlap res_in
+    assert call(res_out=A(0)) == gbf.EINVAL
+    assert call(res_out=ctypes.c_void_p(2 * F + 16)) == gbf.EINVAL
+    assert call(q=A(1)) == gbf.EINVAL
+
+
+def test_qkv_validation(gbf):
+    L = gbf.raw()
+    sec_ok = (ctypes.c_int32 * 3)(44, 42, 42)
+    sec_bad = (ctypes.c_int32 * 3)(44, 42, 41)
+    call = lambda **k: L.gbf_qkv_split_norm_rope(*[k.get(n, d) for n, d in [       # noqa: E731
+        ("qkv", A(0)), ("tokens", 4), ("hq", 2), ("hkv", 1), ("d", 128), ("norm", 0), ("qw", A(1)),
+        ("kw", A(2)), ("eps", 1e-6), ("rope", 0), ("pos", A(3)), ("sec", None), ("theta", 1e4),
+        ("q", A(4)), ("k", A(5)), ("v", A(6)), ("slots", None), ("rows", 4), ("stream", None)]])
+    assert call(tokens=0) == gbf.OK
+    assert call(d=100) == gbf.EUNSUPPORTED
+    assert call(d=512) == gbf.EUNSUPPORTED
+    assert call(d=96, norm=0) == gbf.EUNSUPPORTED          # per-head needs a power of two
+    assert call(norm=5) == gbf.EINVAL
+    assert call(rope=1) == gbf.EINVAL                       # 3D without sections
+    assert call(rope=1, sec=ctypes.cast(sec_bad, ctypes.c_void_p)) == gbf.EINVAL
+    assert call(rope=1, sec=ctypes.cast(sec_ok, ctypes.c_void_p), d=64) == gbf.EINVAL   # sum != head_dim
+    assert call(rows=3) == gbf.EINVAL                       # cache too small without slots
+    assert call(theta=0.0) == gbf.EINVAL
+    assert call(pos=None) == gbf.EINVAL
+    assert call(q=ctypes.c_void_p(5 * F + 4)) == gbf.EALIGN
+    assert call(q=A(0)) == gbf.EINVAL                       # Q overlaps the packed input
+    assert call(k=A(6)) == gbf.EINVAL                       # K and V caches overlap
+
+
+def test_linear_and_fold_and_copy_validation(gbf):
+    L = gbf.raw()
+    lin = lambda **k: L.gbf_linear_bias_gelu(*[k.get(n, d) for n, d in [          # noqa: E731
+        ("x", A(0)), ("w", A(1)), ("b", A(2)), ("y", A(3)), ("m", 128), ("n", 256), ("k", 128), ("act", 1),
+        ("s", None)]])
+    assert lin(m=0) == gbf.OK
+    assert lin(k=100) == gbf.EUNSUPPORTED
+    assert lin(n=8) == gbf.EUNSUPPORTED
+    assert lin(act=3) == gbf.EINVAL
+    assert lin(x=None) == gbf.EINVAL
+    assert lin(y=ctypes.c_void_p(4 * F + 2)) == gbf.EALIGN
+    assert lin(y=A(0)) == gbf.EINVAL
+    fold = lambda **k: L.gbf_bn_fold(*[k.get(n, d) for n, d in [                   # noqa: E731
+        ("w", A(0)), ("b", None), ("g", A(1)), ("be", A(2)), ("mu", A(3)), ("var", A(4)), ("eps", 1e-2),
+        ("oc", 8), ("inner", 27), ("wo", A(5)), ("bo", A(6)), ("s", None)]])
+    assert fold(oc=0) == gbf.OK
+    assert fold(eps=-1.0) == gbf.EINVAL
+    assert fold(inner=0) == gbf.EINVAL
+    assert fold(g=None) == gbf.EINVAL
+    assert fold(bo=A(1)) == gbf.EINVAL                      # b_out overlaps gamma
+    assert fold(wo=ctypes.c_void_p(F + 2)) == gbf.EINVAL    # partial overlap with W
+    assert L.gbf_copy(A(0), A(1), -1, None) == gbf.EINVAL
+    assert L.gbf_copy(A(0), A(1), 0, None) == gbf.OK
+    assert L.gbf_copy(A(0), ctypes.c_void_p(2 * F + 8), 64, None) == gbf.EALIGN
+    assert L.gbf_copy(A(0), ctypes.c_void_p(F + 16), 64, None) == gbf.EINVAL
+
+
+def test_python_binding_raises_with_message(gbf):
+    import torch
+    x = torch.zeros(4, 60, dtype=torch.bfloat16)        # host tensor: validation fails before any launch
+    with pytest.raises(gbf.GbfError) as e:
+        gbf.add_rmsnorm_fp8(x, x, x.clone(), torch.zeros(4, 60, dtype=torch.uint8), gbf.NORM_NOWEIGHT,
+                            stream=type("S", (), {"cuda_stream": 0})())
+    assert e.value.status == gbf.EALIGN

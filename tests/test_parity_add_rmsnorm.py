@@ -1,0 +1,106 @@
+"""GPU parity of gbf_add_rmsnorm_fp8 against the oracle's unfused chain
+(residual add -> bf16 residual -> RMSNorm / _noweight / AdaRMSNorm -> E4M3)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import chains
+from parity import assert_bf16_close, assert_fp8_codes, from_bits, to_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gbf():
+    import fusion_add_rmsnorm_gb300 as g
+    return g
+
+
+def run_gpu(gbf, c, inplace=False):
+    x, res = from_bits(c["x"]), from_bits(c["res"])
+    out = res if inplace else torch.empty_like(res)
+    q = torch.empty(res.shape, dtype=torch.uint8, device="cuda")
+    dev = lambda k: None if c[k] is None else from_bits(c[k])       # noqa: E731
+    gbf.add_rmsnorm_fp8(x, res, out, q, c["mode"], weight=dev("weight"), gate=dev("gate"),
+                        ada_scale=dev("scale"), ada_shift=dev("shift"), eps=c["eps"], fp8_scale=c["s_q"])
+    torch.cuda.synchronize()
+    return to_bits(out), to_bits(q)
+
+
+def run_oracle(c, rows=None):
+    sl = slice(None) if rows is None else rows
+    return chains.add_rmsnorm_fp8(c["x"][sl], c["res"][sl], c["eps"], c["s_q"], c["mode"], weight=c["weight"],
+                                  gate=c["gate"], ada_scale=c["scale"], ada_shift=c["shift"])
+
+
+def check(gbf, c, rows=None, inplace=False, what=""):
+    res_out, q = run_gpu(gbf, c, inplace)
+    ref_res, ref_q = run_oracle(c, rows)
+    if rows is not None:
+        res_out, q = res_out[rows], q[rows]
+    assert_bf16_close(res_out, ref_res, what + " res_out")
+    assert_fp8_codes(q, ref_q, what + " q")
+
+
+def test_tiny_config_residual_rmsnorm_fp8(gbf):
+    """x, res bf16 [16, 256], weight 1 + N(0, 0.1), eps 1e-6, scale 0.05."""
+    check(gbf, workloads.config_tiny_add_rmsnorm(), what="[16,256]")
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("rows,hidden", [(1, 8), (3, 64), (37, 256), (10, 1024), (5, 1032), (7, 4096),
+                                         (3, 8192), (2, 16384), (2, 24576)])
+def test_modes_and_shapes(gbf, mode, gated, rows, hidden):
+    c = workloads.add_rmsnorm_case(rows, hidden, mode, seed=rows * 7 + hidden, gated=gated)
+    check(gbf, c, what=f"mode {mode} gated {gated} [{rows},{hidden}]")
+
+
+def test_in_place_residual(gbf):
+    c = workloads.add_rmsnorm_case(33, 2048, 0, seed=5)
+    check(gbf, c, inplace=True, what="in place")
+
+
+def test_codes_match_worked_example(gbf):
+    """The hand-derived example of tests/golden/rmsnorm_fp8_worked.json (ada, gated)."""
+    import json, os
+    from conftest import GOLDEN
+    g = json.load(open(os.path.join(GOLDEN, "rmsnorm_fp8_worked.json")))["cases"][1]
+    # the kernel needs hidden % 8 == 0: repeat the 4-wide example twice
+    tile = lambda v: torch.tensor(np.tile(np.asarray(v, np.float32), 2)).to(torch.bfloat16)   # noqa: E731
+    c = {"x": to_bits(tile(g["x"][0])[None]), "res": to_bits(tile(g["res"][0])[None]), "mode": 2,
+         "eps": 0.0, "s_q": g["s_q"], "weight": None, "gate": to_bits(tile(g["gate"])),
+         "scale": to_bits(tile(g["scale"])), "shift": to_bits(tile(g["shift"]))}
+    res_out, q = run_gpu(gbf, c)
+    assert res_out.tolist()[0] == g["res_out_bits"][0] * 2
+    assert q.tolist()[0] == g["q_codes"][0] * 2
+
+
+def test_pi05_decoder_chain_180_calls(gbf):
+    """18 layers x 10 steps of the gated AdaRMSNorm + FP8 call on [10, 1024], the
+    residual chaining from call to call on both sides."""
+    w = workloads.pi05_decoder_chain()
+    res_gpu = from_bits(w["res0"])
+    res_ref = w["res0"]
+    xs_gpu = [from_bits(x) for x in w["xs"]]
+    q = torch.empty(res_gpu.shape, dtype=torch.uint8, device="cuda")
+    for call, (gate, shift, scale) in enumerate(w["mods"]):
+        layer = call % w["layers"]
+        nxt = torch.empty_like(res_gpu)
+        gbf.add_rmsnorm_fp8(xs_gpu[layer], res_gpu, nxt, q, 2, gate=from_bits(gate), ada_scale=from_bits(scale),
+                            ada_shift=from_bits(shift), eps=w["eps"], fp8_scale=w["s_q"])
+        res_ref, q_ref = chains.add_rmsnorm_fp8(w["xs"][layer], res_ref, w["eps"], w["s_q"], 2, gate=gate,
+                                                ada_scale=scale, ada_shift=shift)
+        torch.cuda.synchronize()
+        assert_fp8_codes(to_bits(q), q_ref, f"call {call} q")
+        res_gpu = nxt
+    assert_bf16_close(to_bits(res_gpu), res_ref, "final residual")
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_large_sweep_shape_sampled_rows(gbf, mode):
+    """65536 x 4096 in the bench's launch configuration; the oracle checks 64 rows."""
+    c = workloads.add_rmsnorm_case(65536, 4096, mode, seed=11)
+    rows = np.sort(np.random.default_rng(0).choice(65536, 64, replace=False))
+    check(gbf, c, rows=rows, what=f"65536x4096 mode {mode}")

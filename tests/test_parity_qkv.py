@@ -1,0 +1,120 @@
+"""GPU parity of gbf_qkv_split_norm_rope against the oracle's unfused chain
+(split -> Q/K RMSNorm -> RoPE -> Q and K/V-cache writes; V bit for bit)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import chains
+from parity import assert_bf16_close, from_bits, to_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gbf():
+    import fusion_add_rmsnorm_gb300 as g
+    return g
+
+
+def run_gpu(gbf, c, slots=None, cache_rows=None):
+    t, hq, hkv, d = c["tokens"], c["n_q"], c["n_kv"], c["d"]
+    rows = t if cache_rows is None else cache_rows
+    q = torch.empty(t, hq, d, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(rows, hkv, d, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros(rows, hkv, d, dtype=torch.bfloat16, device="cuda")
+    pos = torch.from_numpy(np.ascontiguousarray(c["pos"])).cuda()
+    sl = None if slots is None else torch.from_numpy(np.asarray(slots, np.int32)).cuda()
+    gbf.qkv_split_norm_rope(from_bits(c["qkv"]), hq, hkv, d, c["norm"], from_bits(c["q_w"]), from_bits(c["k_w"]),
+                            c["eps"], c["rope"], pos, c["theta"], q, kc, vc, sections=c["sections"], slots=sl,
+                            cache_rows=rows)
+    torch.cuda.synchronize()
+    return to_bits(q), to_bits(kc), to_bits(vc)
+
+
+def run_oracle(c, tok=None, slots=None, cache_rows=None):
+    sel = slice(None) if tok is None else tok
+    return chains.qkv_split_norm_rope(c["qkv"][sel], c["n_q"], c["n_kv"], c["d"], c["norm"], c["q_w"], c["k_w"],
+                                      c["eps"], c["rope"], c["pos"][sel], c["theta"], sections=c["sections"],
+                                      slots=slots, cache_rows=cache_rows)
+
+
+def check(gbf, c, what, tok=None):
+    q, kc, vc = run_gpu(gbf, c)
+    rq, rk, rv = run_oracle(c, tok)
+    if tok is not None:
+        q, kc, vc = q[tok], kc[tok], vc[tok]
+    assert_bf16_close(q, rq, what + " Q")
+    assert_bf16_close(kc, rk, what + " K")
+    assert np.array_equal(vc, rv), what + " V must be copied bit for bit"
+
+
+def test_qwen3_config_full(gbf):
+    """Packed [4096, 48*128], per-head norm, 1D RoPE theta 1e6 at positions 0..4095."""
+    check(gbf, workloads.config_qwen3_qkv(), "qwen3")
+
+
+def test_wan_config_sampled_tokens(gbf):
+    """Packed [32760, 3*5120] on the 21x30x52 grid, full-width norm, 3D RoPE
+    44/42/42, theta 1e4, in the bench's launch configuration; the oracle checks
+    a sample of 192 tokens (first, last, and random)."""
+    c = workloads.config_wan_qkv()
+    rng = np.random.default_rng(1)
+    tok = np.unique(np.concatenate([[0, 1, 51, 1559, c["tokens"] - 1],
+                                    rng.choice(c["tokens"], 187, replace=False)]))
+    check(gbf, c, "wan", tok)
+
+
+@pytest.mark.parametrize("norm", [0, 1])
+@pytest.mark.parametrize("rope", [0, 1])
+@pytest.mark.parametrize("tokens,hq,hkv,d", [(1, 1, 1, 64), (13, 4, 2, 128), (9, 3, 3, 256), (17, 8, 1, 128),
+                                             (5, 2, 2, 16)])
+def test_all_combinations(gbf, norm, rope, tokens, hq, hkv, d):
+    sections = None
+    grid = None
+    if rope == 1:
+        h = d // 2 // 3 * 2
+        sections = (d - 2 * h, h, h)
+        grid = (3, 4, 5)
+    c = workloads.qkv_case(tokens, hq, hkv, d, norm, rope, seed=tokens + d + 10 * norm + 100 * rope,
+                           theta=1e4, grid=grid, sections=sections)
+    check(gbf, c, f"norm {norm} rope {rope} [{tokens},{hq},{hkv},{d}]")
+
+
+def test_3d_per_head_with_zero_section(gbf):
+    c = workloads.qkv_case(11, 4, 2, 128, 0, 1, seed=3, theta=1e4, grid=(2, 3, 4), sections=(64, 0, 64))
+    check(gbf, c, "3D with an empty section")
+
+
+def test_slots_scatter_into_a_larger_cache(gbf):
+    c = workloads.qkv_case(12, 4, 2, 128, 0, 0, seed=9, theta=1e6)
+    slots = np.random.default_rng(3).permutation(40)[:12].astype(np.int32)
+    q, kc, vc = run_gpu(gbf, c, slots=slots, cache_rows=40)
+    rq, rk, rv = run_oracle(c, slots=slots, cache_rows=40)
+    assert_bf16_close(q, rq, "Q")
+    assert_bf16_close(kc, rk, "K cache")
+    assert np.array_equal(vc, rv)
+    untouched = np.setdiff1d(np.arange(40), slots)
+    assert not kc[untouched].any() and not vc[untouched].any()
+    s, _ = gbf.device_status()
+    assert s == gbf.OK
+
+
+@pytest.mark.parametrize("norm,rope", [(0, 0), (1, 1)])
+def test_out_of_range_slot_is_skipped_and_reported(gbf, norm, rope):
+    """A slot outside the cache writes nothing for that token and raises the
+    device error word; every other token is still written."""
+    grid = (2, 2, 2) if rope else None
+    c = workloads.qkv_case(8, 2, 1, 128, norm, rope, seed=4, theta=1e4, grid=grid,
+                           sections=(44, 42, 42) if rope else None)
+    gbf.device_status()                        # clear
+    slots = np.array([0, 1, 2, 99, 4, 5, 6, 7], np.int32)
+    q, kc, vc = run_gpu(gbf, c, slots=slots, cache_rows=8)
+    s, msg = gbf.device_status()
+    assert s == gbf.EDEVICE and "slot" in msg
+    good = slots != 99
+    rq, rk, rv = run_oracle(c, tok=np.nonzero(good)[0], slots=slots[good], cache_rows=8)
+    assert_bf16_close(q, run_oracle(c)[0], "Q is written for every token")
+    assert_bf16_close(kc[slots[good]], rk[slots[good]], "K")
+    assert not kc[3].any() and not vc[3].any()
+    assert gbf.device_status()[0] == gbf.OK      # cleared by the read
