@@ -1,9 +1,421 @@
-// Linear + bias + GELU(tanh) on tcgen05: placeholder until the kernel lands.
+// linear_bias_gelu: Y = GELU_tanh(X W^T + bias) on the 5th-generation tensor
+// cores (tcgen05), bf16 operands, float32 accumulation in tensor memory (TMEM),
+// bias + GELU applied to the accumulator tile before the single bf16 store.
+//
+// Method: "OpenPPL算子融合深度解析", §4.3 (the epilogue runs on the GEMM's
+// output tile in registers: += bias, then GELU
+// 0.5 a (1 + tanh(0.7978845608 (a + 0.044715 a^3))), then one write) and §3.1
+// (the activation is applied as an epilogue, never as a separate pass); the
+// MatMul -> BiasAdd -> activation pattern of the CANN graph-autofusion article
+// (three HBM passes become one); npu_linear of the MindIE-SD RFC, §3.5.
+//
+// Design (one CTA per SM, persistent):
+//   tiles      BM x BN = 128 x 256 output tile, BK = 64 (one 128-byte swizzle
+//              row of bf16), four tcgen05.mma of M128 N256 K16 per k-block.
+//   warp 0     TMA producer: cp.async.bulk.tensor 2D loads of the X and W
+//              k-blocks into a 4-stage shared-memory ring (128-byte swizzle).
+//   warp 1     MMA issuer: one elected thread issues tcgen05.mma from shared
+//              memory descriptors into a TMEM accumulator and commits each
+//              stage back to the producer with tcgen05.commit.
+//   warp 2     allocates (and at exit frees) 512 TMEM columns: two 128 x 256
+//              float32 accumulators, so the epilogue of tile i overlaps the
+//              MMAs of tile i + 1.
+//   warps 4-7  epilogue: tcgen05.ld 32 columns at a time (warp w reads TMEM
+//              lanes 32 (w % 4) .. +31, one output row per thread), add bias,
+//              GELU, round to bf16, 16-byte stores.
+// Tiles are visited m-fastest, so the CTAs working at one time share one
+// column block of W and all of X, which stay in L2.
+//
+// Every mbarrier wait is bounded (about one second of wall time): a wait that
+// gives up sets DEV_ERR_MBAR_TIMEOUT in the device error word and raises a
+// CTA-wide abort flag; every role then leaves its loop, the MMA issuer drains
+// its outstanding tensor-core work, the producer waits (bounded) for its
+// in-flight copies, and TMEM is freed before the CTA exits.
+#include <cuda.h>
+
+#include "common.cuh"
 #include "kernels.h"
 
 namespace gbf {
-cudaError_t launch_linear_bias_gelu(const GemmArgs&, cudaStream_t, const char** why) {
-  *why = "the tcgen05 GEMM is not built yet";
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;       // 16 KB
+constexpr int B_STAGE_BYTES = BN * BK * 2;       // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int TMEM_COLS = 2 * BN;                // two accumulators
+constexpr int kThreads = 256;
+constexpr int kEpilogueWarp0 = 4;
+constexpr uint64_t kWaitBudgetNs = 1000000000ull;   // one second
+
+struct __align__(8) SharedCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + sizeof(SharedCtl);
+
+// ------------------------------------------------------------ PTX wrappers
+
+GBF_DEVICE uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+GBF_DEVICE uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
+
+GBF_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+GBF_DEVICE void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+GBF_DEVICE void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+GBF_DEVICE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity to complete.
+// Returns false (after flagging the error and the CTA abort) when it gives up
+// or when another role already aborted.
+GBF_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, SharedCtl* ctl, unsigned int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
+      if (global_timer() - t0 > kWaitBudgetNs) {
+        raise_error(err, DEV_ERR_MBAR_TIMEOUT);
+        *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
+        return false;
+      }
+    }
+  }
+}
+
+GBF_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+GBF_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+GBF_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+GBF_DEVICE void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, float32 accumulator).
+GBF_DEVICE void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 consecutive float32 columns of this warp's 32 TMEM lanes, one lane per thread.
+GBF_DEVICE void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row core groups 1024 bytes apart
+// (stride byte offset), descriptor version 1, layout "swizzle 128B".
+GBF_DEVICE uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);          // start address
+  d |= static_cast<uint64_t>(1) << 16;                          // leading byte offset (unused for SW128 K-major)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                  // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                          // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                          // swizzle 128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: float32 D, bf16 A and B, both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+GBF_DEVICE float gelu_tanh(float a) {
+  const float inner = 0.7978845608f * fmaf(0.044715f * a, a * a, a);
+  return 0.5f * a * (1.0f + tanhf(inner));
+}
+
+struct GemmParams {
+  const __nv_bfloat16* bias;
+  __nv_bfloat16* y;
+  unsigned int* err;
+  int m, n, k;
+  int m_tiles, n_tiles;
+  int act;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                        const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem_a = smem;                                   // STAGES x 16 KB
+  uint8_t* smem_b = smem + STAGES * A_STAGE_BYTES;          // STAGES x 32 KB
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + STAGES * STAGE_BYTES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = p.m_tiles * p.n_tiles;
+  const int k_blocks = p.k / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&ctl->tmem_full[a], 1);
+      mbar_init(&ctl->tmem_empty[a], 4);     // one arrive per epilogue warp
+    }
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&ctl->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued[STAGES] = {};        // phases issued per stage (for the final drain)
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile % p.m_tiles) * BM;
+        const int n0 = (tile / p.m_tiles) * BN;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, ctl, p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
+          tma_load_2d(smem_a + stage * A_STAGE_BYTES, &map_x, &ctl->full[stage], kb * BK, m0);
+          tma_load_2d(smem_b + stage * B_STAGE_BYTES, &map_w, &ctl->full[stage], kb * BK, n0);
+          ++issued[stage];
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every issued copy has landed before the CTA may exit: wait for the
+      // last phase issued on each stage (bounded; immediate on the normal path).
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s]) mbar_wait(&ctl->full[s], (issued[s] - 1) & 1u, ctl, p.err);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1u;
+        if (!mbar_wait(&ctl->tmem_empty[acc], acc_phase ^ 1u, ctl, p.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!mbar_wait(&ctl->full[stage], phase, ctl, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem_a + stage * A_STAGE_BYTES);
+          const uint32_t b_addr = smem_u32(smem_b + stage * B_STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // advance 16 elements (32 bytes) along K inside the swizzled row
+            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * UMMA_K * 2);
+            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * UMMA_K * 2);
+            tc_mma(d_tmem, a_desc, b_desc, kIdesc, (kb | kk) != 0);
+          }
+          tc_commit(&ctl->empty[stage]);      // frees the stage once these MMAs have read it
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) tc_commit(&ctl->tmem_full[acc]);
+      }
+      // Drain: all tensor-core work this thread issued has completed.
+      tc_commit(&ctl->drain);
+      mbar_wait(&ctl->drain, 0, ctl, p.err);
+    }
+  } else if (warp >= kEpilogueWarp0) {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp - kEpilogueWarp0;          // TMEM lanes 32*quarter .. +31
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1u;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&ctl->tmem_full[acc], acc_phase, ctl, p.err);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const int m0 = (tile % p.m_tiles) * BM;
+      const int n0 = (tile / p.m_tiles) * BN;
+      const int row = m0 + quarter * 32 + lane;
+      __nv_bfloat16* yrow = p.y + static_cast<int64_t>(row) * p.n;
+      const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(taddr + c * 32, r);
+        const int col0 = n0 + c * 32;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int col = col0 + g * 8;
+          if (col >= p.n) break;                          // N % 16 == 0: whole 8-column groups
+          float v[8];
+          float bz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (p.bias) bf16x8_to_f32(ld_cached(p.bias + col), bz);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float a = __uint_as_float(r[g * 8 + e]) + bz[e];
+            v[e] = p.act == kActGeluTanh ? gelu_tanh(a) : a;
+          }
+          if (row < p.m) st_16(yrow + col, f32x8_to_bf16x8(v));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->tmem_empty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------- host: tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2D bf16 tensor [rows, cols] (cols contiguous), box [box_rows, 64], 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, const char** why) {
+  CUtensorMap map_x, map_w;
+  if (!make_map(&map_x, a.x, a.m, a.k, BM) || !make_map(&map_w, a.w, a.n, a.k, BN)) {
+    *why = "cuTensorMapEncodeTiled is unavailable or rejected the operands";
+    return cudaErrorInvalidValue;
+  }
+  GemmParams p;
+  p.bias = static_cast<const __nv_bfloat16*>(a.bias);
+  p.y = static_cast<__nv_bfloat16*>(a.y);
+  p.err = a.err;
+  p.m = static_cast<int>(a.m);
+  p.n = static_cast<int>(a.n);
+  p.k = static_cast<int>(a.k);
+  p.m_tiles = static_cast<int>((a.m + BM - 1) / BM);
+  p.n_tiles = static_cast<int>((a.n + BN - 1) / BN);
+  p.act = a.act;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int grid = tiles < sms ? tiles : sms;
+  cudaError_t e = cudaFuncSetAttribute(linear_bias_gelu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) {
+    *why = "could not reserve shared memory";
+    return e;
+  }
+  linear_bias_gelu_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_x, map_w, p);
+  return cudaGetLastError();
+}
+
 }  // namespace gbf

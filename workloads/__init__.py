@@ -149,3 +149,11 @@ def config_linear_gelu(seed=0):
     """Linear + bias + GELU(tanh): X [8192, 4096], W [16384, 4096], bias [16384],
     plus the BN-fold parameters of W's 16384 output channels."""
     return linear_gelu_case(8192, 16384, 4096, seed)
+
+
+def as_torch(bits, device="cuda"):
+    """numpy storage bits (uint16 bf16 / uint8 / int32 / float32) -> torch tensor on `device`."""
+    a = np.ascontiguousarray(bits)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(a).to(device)
