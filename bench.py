@@ -132,9 +132,11 @@ class AddRmsNormOp(Op):
 
 
 class AdaChainOp(Op):
-    """180 sequential calls (18 layers x 10 steps) on [10, 1024]."""
+    """180 sequential calls (18 layers x 10 steps) on [10, 1024], captured once
+    through the C ABI into a CUDA graph (with the calls' programmatic-dependent
+    launch edges) and replayed as one submission per step."""
 
-    def __init__(self, gbf, seed=0):
+    def __init__(self, gbf, seed=0, graph=True):
         import torch
         import workloads
         from workloads import as_torch as from_bits
@@ -147,8 +149,26 @@ class AdaChainOp(Op):
         self.mods = [tuple(from_bits(m) for m in mod) for mod in w["mods"]]
         self.bufs = [torch.empty_like(self.res0), torch.empty_like(self.res0)]
         self.q = torch.empty(self.res0.shape, dtype=torch.uint8, device="cuda")
+        self.graph = None
+        if graph:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                self.run_eager()
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph):
+                self.run_eager()
+            torch.cuda.synchronize()
 
     def run(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.run_eager()
+
+    def run_eager(self):
         res = self.res0
         L = self.w["layers"]
         for call, (gate, shift, scale) in enumerate(self.mods):
@@ -272,70 +292,133 @@ class FoldOp(Op):
         return [self.w, self.b, self.g, self.be, self.mu, self.var], [self.wo, self.bo]
 
 
-def build_ops(gbf, with_gemm):
+OP_NAMES = ("add_rmsnorm_fp8", "pi05_ada_chain", "sweep_weighted", "sweep_noweight", "sweep_ada", "qwen3_qkv",
+            "wan_qkv3d", "linear_bias_gelu", "bn_fold")
+
+
+def build_ops(gbf, with_gemm, only=None, small=False):
+    """The step's operators.  `small` shrinks the large ones to profiling size
+    (inputs still larger than L2) for ncu captures; `only` keeps a subset."""
     import workloads
-    ops = [AddRmsNormOp(gbf, "add_rmsnorm_fp8", 16, 256, 0, False, 0),
-           AdaChainOp(gbf),
-           AddRmsNormOp(gbf, "sweep_weighted", 65536, 4096, 0, False, 11),
-           AddRmsNormOp(gbf, "sweep_noweight", 65536, 4096, 1, False, 12),
-           AddRmsNormOp(gbf, "sweep_ada", 65536, 4096, 2, True, 13),
-           QkvOp(gbf, "qwen3_qkv", workloads.config_qwen3_qkv()),
-           QkvOp(gbf, "wan_qkv3d", workloads.config_wan_qkv())]
-    lin = workloads.config_linear_gelu()
-    if with_gemm:
-        ops.append(GemmOp(gbf, lin))
-    ops.append(FoldOp(gbf, lin))
+    want = set(only or OP_NAMES)
+    rows = 8192 if small else 65536
+    ops = []
+    if "add_rmsnorm_fp8" in want:
+        ops.append(AddRmsNormOp(gbf, "add_rmsnorm_fp8", 16, 256, 0, False, 0))
+    if "pi05_ada_chain" in want:
+        ops.append(AdaChainOp(gbf))
+    for name, mode, gated, seed in (("sweep_weighted", 0, False, 11), ("sweep_noweight", 1, False, 12),
+                                    ("sweep_ada", 2, True, 13)):
+        if name in want:
+            ops.append(AddRmsNormOp(gbf, name, rows, 4096, mode, gated, seed))
+    if "qwen3_qkv" in want:
+        ops.append(QkvOp(gbf, "qwen3_qkv", workloads.config_qwen3_qkv()))
+    if "wan_qkv3d" in want:
+        ops.append(QkvOp(gbf, "wan_qkv3d", workloads.config_wan_qkv(tokens=4096 if small else None)))
+    if want & {"linear_bias_gelu", "bn_fold"}:
+        lin = workloads.linear_gelu_case(2048, 16384, 4096) if small else workloads.config_linear_gelu()
+        if with_gemm and "linear_bias_gelu" in want:
+            ops.append(GemmOp(gbf, lin))
+        if "bn_fold" in want:
+            ops.append(FoldOp(gbf, lin))
     return ops
 
 
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    """SM clock, power and throttle reasons sampled every 10 ms while the timed
+    region runs, read from NVML (libnvidia-ml, through ctypes); falls back to
+    nvidia-smi at 50 ms when NVML cannot be loaded."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index):
-        self.index, self.proc, self.lines = index, None, []
+    def __init__(self, cuda_index):
+        self.cuda_index = cuda_index
+        self.samples, self.first, self.stop_flag = [], 0, False
+        self.nvml, self.dev, self.max_mhz, self.thread, self.proc = None, None, None, None, None
+
+    def _open_nvml(self):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return False
+        props = torch.cuda.get_device_properties(self.cuda_index)
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+        dev = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(dev)) != 0:
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.cuda_index), ctypes.byref(dev)) != 0:
+                return False
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx))
+        self.nvml, self.dev, self.max_mhz = lib, dev, float(mx.value)
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return True
+
+    def _poll(self):
+        import ctypes
+        clk, rea, pw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        while not self.stop_flag:
+            self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk))
+            self.reasons_fn(self.dev, ctypes.byref(rea))
+            self.nvml.nvmlDeviceGetPowerUsage(self.dev, ctypes.byref(pw))
+            self.samples.append((float(clk.value), int(rea.value), pw.value / 1000.0))
+            time.sleep(0.01)
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+            ok = self._open_nvml()
+        except (OSError, AttributeError):
+            ok = False
+        if ok:
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.cuda_index),
+                                          "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active,power.draw",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            threading.Thread(target=self._read, daemon=True).start()
+            threading.Thread(target=self._read_smi, daemon=True).start()
         except OSError:
             self.proc = None
 
-    def _read(self):
+    def _read_smi(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            f = [x.strip() for x in line.split(",")]
+            try:
+                self.max_mhz = float(f[1])
+                self.samples.append((float(f[0]), int(f[2], 16), float(f[3])))
+            except (ValueError, IndexError):
+                continue
+
+    def mark(self):
+        """Start of the timed region: keep samples from here on (and the one before)."""
+        t0 = time.time()
+        while (self.thread or self.proc) and not self.samples and time.time() - t0 < 5:
+            time.sleep(0.01)
+        self.first = max(0, len(self.samples) - 1)
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 8:
-                continue
-            try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        self.stop_flag = True
+        if self.thread is not None:
+            self.thread.join(timeout=1)
+        if self.proc is not None:
+            self.proc.terminate()
+        got = self.samples[self.first:]
+        if not got:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no clock samples"], "samples": 0}
+        reasons = set()
+        for _, r, _ in got:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(c for c, _, _ in got), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(got),
+                "power_w_max": round(max(p for _, _, p in got), 1),
+                "source": "nvml" if self.thread is not None else "nvidia-smi"}
 
 
 # ------------------------------------------------------------- traffic record
@@ -388,7 +471,7 @@ def cpu_baseline_sample(scale=1):
     w = workloads.pi05_decoder_chain()
     r = w["res0"]
 
-    n_calls = 10 * scale
+    n_calls = min(10 * scale, 180)
 
     def chain10():
         nonlocal r
@@ -430,7 +513,7 @@ def cpu_baseline_sample(scale=1):
                        for k, (b, dt) in res.items()}}
 
 
-def run_cpu_baseline(scale=8):
+def run_cpu_baseline(scale=32):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_cpu-baseline-child", str(scale)], env=env,
@@ -439,7 +522,7 @@ def run_cpu_baseline(scale=8):
         return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": r.stderr[-300:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": round(d["gbs"], 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": (f"float64 numpy oracle, one thread: [16,256] add+RMSNorm+FP8; {10 * scale} of the 180 "
+            "sample": (f"float64 numpy oracle, one thread: [16,256] add+RMSNorm+FP8; {min(10 * scale, 180)} of the 180 "
                        f"chained [10,1024] AdaRMSNorm calls; {64 * scale} rows of each [65536,4096] sweep; "
                        f"{256 * scale} Qwen3 tokens; {64 * scale} Wan tokens; BN fold of {1024 * scale} channels; "
                        "GB/s = algorithmic bytes / oracle time over the memory-bound operators (a "
@@ -491,7 +574,7 @@ def main_gpu(args):
     import fusion_add_rmsnorm_gb300 as gbf
     peaks = load_peaks()
     with_gemm = not args.no_gemm
-    ops = build_ops(gbf, with_gemm)
+    ops = build_ops(gbf, with_gemm, args.only.split(",") if args.only else None, args.small)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -506,6 +589,8 @@ def main_gpu(args):
             record.append((op, e0, e1))
         return times
 
+    clocks = ClockSampler(local)
+    clocks.start()
     for _ in range(args.warmup):
         one_step([])
     torch.cuda.synchronize()
@@ -513,10 +598,9 @@ def main_gpu(args):
     if status != gbf.OK:
         raise RuntimeError(f"device status after warm-up: {msg}")
 
-    clocks = ClockSampler(local)
     barrier(pg)
     torch.cuda.synchronize()
-    clocks.start()
+    clocks.mark()
     t_wall0 = time.perf_counter()
     recs = []
     for _ in range(args.steps):
@@ -554,10 +638,11 @@ def main_gpu(args):
     mem_ms_max = max_over_ranks(pg, mem_ms)
     step_ms_max = max_over_ranks(pg, step_ms)
     total_bytes = sum_over_ranks(pg, mem_bytes)
-    value = total_bytes / (mem_ms_max / 1e3) / 1e9
+    value = total_bytes / (mem_ms_max / 1e3) / 1e9 if mem_ms_max > 0 else 0.0
 
     # dominant memory-bound kernel (largest share of the step) -> roofline
-    mem_ops = [(n, d) for n, d in out_ops.items() if "gbs" in d]
+    mem_ops = [(n, d) for n, d in out_ops.items() if "gbs" in d] or [(n, dict(d, gbs=0.0))
+                                                                   for n, d in out_ops.items()]
     dom_name, dom = max(mem_ops, key=lambda kv: kv[1]["ms"])
     dom_op = per_op[dom_name]["op"]
     roofline = {"kernel": dom_name, "bound": "hbm", "achieved": dom["gbs"], "peak": peaks["hbm_gbs"],
@@ -585,10 +670,11 @@ def main_gpu(args):
                                  "traffic": kernel_traffic("gemm_tcgen05.cu", 1)}
 
     # end to end through the C ABI with host buffers: H2D inputs, op, D2H outputs
-    e2e = measure_e2e(ops, args, stream)
-    e2e_ms = max_over_ranks(pg, e2e["mem_ms"])
-    line["e2e"] = {"value": round(sum_over_ranks(pg, e2e["mem_bytes"]) / (e2e_ms / 1e3) / 1e9, 1), "unit": UNIT,
-                   "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
+    if not args.no_e2e:
+        e2e = measure_e2e(ops, args, stream)
+        e2e_ms = max_over_ranks(pg, e2e["mem_ms"])
+        line["e2e"] = {"value": round(sum_over_ranks(pg, e2e["mem_bytes"]) / (e2e_ms / 1e3) / 1e9, 1),
+                       "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = run_cpu_baseline()
     if rank == 0:
@@ -664,11 +750,14 @@ def main_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-gemm", action="store_true", help="leave the GEMM row out of the step")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--only", default="", help="comma-separated subset of: " + ", ".join(OP_NAMES))
+    ap.add_argument("--small", action="store_true", help="profiling-size cases (still larger than L2)")
     ap.add_argument("--_cpu-baseline-child", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args._cpu_baseline_child:

@@ -12,7 +12,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/gbfuse.h"
+#include "gbfuse.h"
 #include "common.cuh"
 #include "kernels.h"
 

@@ -9,117 +9,191 @@
 // §3.3.
 //
 // Layout: a row (token) of H bf16 values is split into H/8 16-byte vectors.
-// A group of TPR threads (a power of two, 8..1024) owns one row; each thread
+// A group of TPR threads (a power of two, 8..512) owns one row; each thread
 // owns NV vectors strided by TPR, so one warp instruction touches TPR*16
-// contiguous bytes.  The row is held in registers as the rounded bf16 residual
-// (half the registers of float32) between the reduction and the output pass,
-// so HBM sees x and res once and res_out and the codes once.
+// contiguous bytes.  CTAs are persistent: a CTA walks rows with a grid-sized
+// stride, keeps its columns' weight factors in registers for the whole launch,
+// and loads the next row's x and res while it reduces and writes the current
+// one.
 //
-// Rounding points: r = x + res (or res + gate*x) in float32 -> res_out =
-// bf16_rne(r) -> the norm reads that bf16 value -> y = r_hat * inv * w (or
-// * (1 + scale) + shift) in float32, never stored -> code = e4m3_rne_sat(y / s).
+// Rounding points: res_out = bf16(x + res) or bf16(res + gate * x), one
+// rounding of the exact value (bf16x2 add / fused multiply-add); the norm reads
+// that bf16 value; y = r_hat * inv * w (or * (1 + scale) + shift) stays in
+// float32 registers with the descale 1/s folded into the per-column factors;
+// code = e4m3_rne_sat(y / s).
 #include "common.cuh"
 #include "kernels.h"
 
 namespace gbf {
 namespace {
 
-constexpr int kMaxBlock = 1024;
+constexpr int kMaxBlock = 512;
+
+GBF_DEVICE uint4 bf16x8_add(uint4 a, uint4 b) {
+  uint4 r;
+  const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+  __nv_bfloat162* pr = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) pr[i] = __hadd2(pa[i], pb[i]);
+  return r;
+}
+
+// g * x + r per element, one rounding
+GBF_DEVICE uint4 bf16x8_fma(uint4 g, uint4 x, uint4 r0) {
+  uint4 r;
+  const __nv_bfloat162* pg = reinterpret_cast<const __nv_bfloat162*>(&g);
+  const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&x);
+  const __nv_bfloat162* pr0 = reinterpret_cast<const __nv_bfloat162*>(&r0);
+  __nv_bfloat162* pr = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) pr[i] = __hfma2(pg[i], px[i], pr0[i]);
+  return r;
+}
 
 template <int MODE, bool GATED, int NV>
 __global__ void __launch_bounds__(kMaxBlock)
 add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
+  // Rows of up to 2 vectors per thread keep the per-column factors and the
+  // next row's inputs in registers; wider rows (BIG) reload the factors from
+  // L1 and issue their loads at the top of each row to stay within registers.
+  constexpr bool BIG = NV > 2;
   const int tpr = a.tpr;
   const int lane = threadIdx.x & (tpr - 1);
   const int row_in_cta = threadIdx.x / tpr;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta + row_in_cta;
-  const bool row_ok = row < a.rows;
   const int nvec = static_cast<int>(a.hidden >> 3);
-  const int64_t base = row * a.hidden;
+  const int64_t row_stride = static_cast<int64_t>(gridDim.x) * a.rows_per_cta;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
+  const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(a.res_in);
+  __nv_bfloat16* res_out = static_cast<__nv_bfloat16*>(a.res_out);
+  uint8_t* q_out = static_cast<uint8_t*>(a.q_out);
+  const float rs = 1.0f / a.fp8_scale;
 
   pdl_wait();
 
-  uint4 xr[NV], rr[NV];
+  bool vok[NV];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int v = lane + k * tpr;
-    if (row_ok && v < nvec) {
-      xr[k] = ld_stream(static_cast<const __nv_bfloat16*>(a.x) + base + v * 8);
-      rr[k] = ld_stream(static_cast<const __nv_bfloat16*>(a.res_in) + base + v * 8);
+  for (int k = 0; k < NV; ++k) vok[k] = lane + k * tpr < nvec;
+
+  // Per-column factors (descale folded in):
+  //   WEIGHT: fa = w / s;  NOWEIGHT: none;  ADA: fa = (1 + scale) / s, fb = shift / s.
+  auto factors = [&](int k, float* fa, float* fb) {
+    const int col = (lane + k * tpr) * 8;
+    if (MODE == kNormWeight) {
+      float w[8];
+      bf16x8_to_f32(ld_cached(static_cast<const __nv_bfloat16*>(a.weight) + col), w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) fa[i] = w[i] * rs;
+    } else if (MODE == kNormAda) {
+      float sc[8], sh[8];
+      bf16x8_to_f32(ld_cached(static_cast<const __nv_bfloat16*>(a.ada_scale) + col), sc);
+      bf16x8_to_f32(ld_cached(static_cast<const __nv_bfloat16*>(a.ada_shift) + col), sh);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        fa[i] = (1.0f + sc[i]) * rs;
+        fb[i] = sh[i] * rs;
+      }
+    }
+  };
+  constexpr int NF = BIG ? 1 : NV;
+  float fa[NF][8], fb[NF][8];
+  uint4 gate[NF];
+  if (!BIG) {
+#pragma unroll
+    for (int k = 0; k < NF; ++k) {
+      if (!vok[k]) continue;
+      if (GATED) gate[k] = ld_cached(static_cast<const __nv_bfloat16*>(a.gate) + (lane + k * tpr) * 8);
+      factors(k, fa[k], fb[k]);
     }
   }
+
+  int64_t row = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta + row_in_cta;
+  uint4 xr[NV], rr[NV];
+  auto load_row = [&](int64_t r) {
+    if (r < a.rows) {
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (vok[k]) {
+          const int64_t off = r * a.hidden + (lane + k * tpr) * 8;
+          xr[k] = ld_stream(x + off);
+          rr[k] = ld_stream(res + off);
+        }
+    }
+  };
+  if (!BIG) load_row(row);
   pdl_launch_dependents();
 
-  // r = x + res (or res + gate*x) -> res_out = bf16(r); sum of r_hat^2.
-  uint4 rh[NV];
-  float sumsq = 0.f;
+  __shared__ float part[kMaxBlock / 32];
+  const int warp = threadIdx.x >> 5;
+  const int wpr = tpr >> 5;                        // warps per row (when tpr > 32)
+  const int first_warp = tpr > 32 ? (warp / wpr) * wpr : 0;
+  // every thread of the CTA runs the same number of trips (the reduction syncs)
+  const int64_t rows_cta0 = a.rows - static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
+  const int64_t trips = rows_cta0 <= 0 ? 0 : (rows_cta0 + row_stride - 1) / row_stride;
+
+  for (int64_t trip = 0; trip < trips; ++trip, row += row_stride) {
+    const bool row_ok = row < a.rows;
+    uint4 cx[NV], cr[NV];
+    if (BIG) load_row(row);
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int v = lane + k * tpr;
-    if (row_ok && v < nvec) {
-      float xf[8], rf[8], o[8];
-      bf16x8_to_f32(xr[k], xf);
-      bf16x8_to_f32(rr[k], rf);
-      if (GATED) {
-        float gf[8];
-        bf16x8_to_f32(ld_cached(static_cast<const __nv_bfloat16*>(a.gate) + v * 8), gf);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = fmaf(gf[i], xf[i], rf[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = xf[i] + rf[i];
-      }
-      rh[k] = f32x8_to_bf16x8(o);
-      st_16(static_cast<__nv_bfloat16*>(a.res_out) + base + v * 8, rh[k]);
-      float h[8];
-      bf16x8_to_f32(rh[k], h);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sumsq = fmaf(h[i], h[i], sumsq);
+    for (int k = 0; k < NV; ++k) {
+      cx[k] = xr[k];
+      cr[k] = rr[k];
     }
-  }
+    if (!BIG) load_row(row + row_stride);          // next row in flight during this one
 
-  // Row reduction: shuffles inside the row's lanes, shared memory across warps.
-  sumsq = group_sum(sumsq, tpr < 32 ? tpr : 32);
-  if (tpr > 32) {
-    __shared__ float part[kMaxBlock / 32];
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) part[warp] = sumsq;
-    __syncthreads();
-    const int wpr = tpr >> 5;               // warps per row
-    const int first = (warp / wpr) * wpr;
-    float s = 0.f;
-    for (int w = 0; w < wpr; ++w) s += part[first + w];
-    sumsq = s;
-  }
-  if (!row_ok) return;
-
-  // inv = 1/sqrt(mean + eps); the descale 1/s is folded into the row factor.
-  const float inv = 1.0f / sqrtf(sumsq / static_cast<float>(a.hidden) + a.eps);
-  const float rs = 1.0f / a.fp8_scale;
-  const float row_factor = inv * rs;
-
+    uint4 rh[NV];
+    float sumsq = 0.f;
+    if (row_ok) {
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int v = lane + k * tpr;
-    if (v < nvec) {
+      for (int k = 0; k < NV; ++k) {
+        if (!vok[k]) continue;
+        if (GATED) {
+          const uint4 g = BIG ? ld_cached(static_cast<const __nv_bfloat16*>(a.gate) + (lane + k * tpr) * 8)
+                              : gate[BIG ? 0 : k];
+          rh[k] = bf16x8_fma(g, cx[k], cr[k]);
+        } else {
+          rh[k] = bf16x8_add(cx[k], cr[k]);
+        }
+        st_16(res_out + row * a.hidden + (lane + k * tpr) * 8, rh[k]);
+        float h[8];
+        bf16x8_to_f32(rh[k], h);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sumsq = fmaf(h[i], h[i], sumsq);
+      }
+    }
+    sumsq = group_sum(sumsq, tpr < 32 ? tpr : 32);
+    if (tpr > 32) {
+      if ((threadIdx.x & 31) == 0) part[warp] = sumsq;
+      __syncthreads();
+      float s = 0.f;
+      for (int w = 0; w < wpr; ++w) s += part[first_warp + w];
+      sumsq = s;
+      __syncthreads();                             // part[] is rewritten next trip
+    }
+    if (!row_ok) continue;
+    const float inv = 1.0f / sqrtf(sumsq / static_cast<float>(a.hidden) + a.eps);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (!vok[k]) continue;
       float h[8], q[8];
       bf16x8_to_f32(rh[k], h);
+      float fbig_a[8], fbig_b[8];
+      const float* fak = BIG ? fbig_a : fa[BIG ? 0 : k];
+      const float* fbk = BIG ? fbig_b : fb[BIG ? 0 : k];
+      if (BIG) factors(k, fbig_a, fbig_b);
       if (MODE == kNormWeight) {
-        float wf[8];
-        bf16x8_to_f32(ld_cached(static_cast<const __nv_bfloat16*>(a.weight) + v * 8), wf);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = (h[i] * row_factor) * wf[i];
+        for (int i = 0; i < 8; ++i) q[i] = (h[i] * inv) * fak[i];
       } else if (MODE == kNormNoWeight) {
+        const float f = inv * rs;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = h[i] * row_factor;
+        for (int i = 0; i < 8; ++i) q[i] = h[i] * f;
       } else {
-        float sc[8], sh[8];
-        bf16x8_to_f32(ld_cached(static_cast<const __nv_bfloat16*>(a.ada_scale) + v * 8), sc);
-        bf16x8_to_f32(ld_cached(static_cast<const __nv_bfloat16*>(a.ada_shift) + v * 8), sh);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = fmaf(h[i] * inv, 1.0f + sc[i], sh[i]) * rs;
+        for (int i = 0; i < 8; ++i) q[i] = fmaf(h[i] * inv, fak[i], fbk[i]);
       }
-      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.q_out) + base + v * 8) = f32x8_to_e4m3x8(q);
+      *reinterpret_cast<uint2*>(q_out + row * a.hidden + (lane + k * tpr) * 8) = f32x8_to_e4m3x8(q);
     }
   }
 }
@@ -139,8 +213,20 @@ cudaError_t launch_mode(const AddRmsNormArgs& a, int nv, dim3 grid, dim3 block, 
     case 1: return cudaLaunchKernelEx(&cfg, add_rmsnorm_fp8_kernel<MODE, GATED, 1>, a);
     case 2: return cudaLaunchKernelEx(&cfg, add_rmsnorm_fp8_kernel<MODE, GATED, 2>, a);
     case 4: return cudaLaunchKernelEx(&cfg, add_rmsnorm_fp8_kernel<MODE, GATED, 4>, a);
+    case 8: return cudaLaunchKernelEx(&cfg, add_rmsnorm_fp8_kernel<MODE, GATED, 8>, a);
     default: return cudaErrorInvalidValue;
   }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
 }
 
 }  // namespace
@@ -148,8 +234,9 @@ cudaError_t launch_mode(const AddRmsNormArgs& a, int nv, dim3 grid, dim3 block, 
 AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden) {
   AddRmsNormPlan p = {};
   const int64_t nvec = hidden / 8;
+  // Up to 512 threads per row, then more vectors per thread.
   int nv = 1;
-  while (nv < 4 && nvec > static_cast<int64_t>(nv) * kMaxBlock) nv *= 2;
+  while (nv < 8 && nvec > static_cast<int64_t>(nv) * kMaxBlock) nv *= 2;
   int tpr = 8;
   while (static_cast<int64_t>(tpr) * nv < nvec) tpr *= 2;
   p.ok = static_cast<int64_t>(tpr) * nv >= nvec && tpr <= kMaxBlock;
@@ -157,8 +244,11 @@ AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden) {
   p.tpr = tpr;
   // Small rows share a CTA of 256 threads; large rows get a CTA each.
   p.rows_per_cta = tpr >= 256 ? 1 : 256 / tpr;
-  p.grid = rows == 0 ? 0 : (rows + p.rows_per_cta - 1) / p.rows_per_cta;
   p.block = tpr * p.rows_per_cta;
+  const int64_t blocks = rows == 0 ? 0 : (rows + p.rows_per_cta - 1) / p.rows_per_cta;
+  // Persistent: at most 2048 / block CTAs per SM.
+  const int64_t cap = static_cast<int64_t>(sm_count()) * (2048 / p.block);
+  p.grid = blocks < cap ? blocks : cap;
   return p;
 }
 

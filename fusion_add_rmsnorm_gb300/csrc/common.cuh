@@ -101,6 +101,16 @@ GBF_DEVICE float group_sum(float v, int width) {
   return v;
 }
 
+// Sum over the aligned segment of `width` lanes (a power of two <= 32) that
+// holds this lane; only that segment's lanes take part, so segments of one
+// warp may follow different control paths.
+GBF_DEVICE float segment_sum(float v, int width) {
+  const unsigned lane = threadIdx.x & 31u;
+  const unsigned seg = width >= 32 ? 0xffffffffu : (((1u << width) - 1u) << (lane & ~static_cast<unsigned>(width - 1)));
+  for (int o = width >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(seg, v, o);
+  return v;
+}
+
 // --------------------------------------------- programmatic dependent launch
 
 // Wait until the grids this launch depends on have completed and their

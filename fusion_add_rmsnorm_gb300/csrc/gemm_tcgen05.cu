@@ -33,8 +33,8 @@
 // in-flight copies, and TMEM is freed before the CTA exits.
 #include <cuda.h>
 
-#include "common.cuh"
 #include "kernels.h"
+#include "tma.cuh"
 
 namespace gbf {
 namespace {
@@ -50,7 +50,6 @@ constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;                // two accumulators
 constexpr int kThreads = 256;
 constexpr int kEpilogueWarp0 = 4;
-constexpr uint64_t kWaitBudgetNs = 1000000000ull;   // one second
 
 struct __align__(8) SharedCtl {
   uint64_t full[STAGES];
@@ -65,58 +64,6 @@ struct __align__(8) SharedCtl {
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + sizeof(SharedCtl);
 
 // ------------------------------------------------------------ PTX wrappers
-
-GBF_DEVICE uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-
-GBF_DEVICE uint64_t global_timer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-GBF_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-GBF_DEVICE void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-GBF_DEVICE void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-GBF_DEVICE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of `bar` with the given parity to complete.
-// Returns false (after flagging the error and the CTA abort) when it gives up
-// or when another role already aborted.
-GBF_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, SharedCtl* ctl, unsigned int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
-      if (global_timer() - t0 > kWaitBudgetNs) {
-        raise_error(err, DEV_ERR_MBAR_TIMEOUT);
-        *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
-        return false;
-      }
-    }
-  }
-}
 
 GBF_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
   asm volatile(
@@ -214,7 +161,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
     }
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
   }
@@ -240,7 +187,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
         const int m0 = (tile % p.m_tiles) * BM;
         const int n0 = (tile / p.m_tiles) * BN;
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, ctl, p.err)) {
+          if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, &ctl->abort, p.err)) {
             ok = false;
             break;
           }
@@ -256,8 +203,9 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       }
       // Every issued copy has landed before the CTA may exit: wait for the
       // last phase issued on each stage (bounded; immediate on the normal path).
+      int drain_abort = 0;                 // own flag: the CTA one may already be set
       for (int s = 0; s < STAGES; ++s)
-        if (issued[s]) mbar_wait(&ctl->full[s], (issued[s] - 1) & 1u, ctl, p.err);
+        if (issued[s]) mbar_wait(&ctl->full[s], (issued[s] - 1) & 1u, &drain_abort, nullptr);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -269,11 +217,11 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1u;
-        if (!mbar_wait(&ctl->tmem_empty[acc], acc_phase ^ 1u, ctl, p.err)) break;
+        if (!mbar_wait(&ctl->tmem_empty[acc], acc_phase ^ 1u, &ctl->abort, p.err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!mbar_wait(&ctl->full[stage], phase, ctl, p.err)) {
+          if (!mbar_wait(&ctl->full[stage], phase, &ctl->abort, p.err)) {
             ok = false;
             break;
           }
@@ -297,7 +245,8 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       }
       // Drain: all tensor-core work this thread issued has completed.
       tc_commit(&ctl->drain);
-      mbar_wait(&ctl->drain, 0, ctl, p.err);
+      int drain_abort = 0;
+      mbar_wait(&ctl->drain, 0, &drain_abort, p.err);
     }
   } else if (warp >= kEpilogueWarp0) {
     // ------------------------------------------------------------ epilogue
@@ -307,7 +256,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1u;
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&ctl->tmem_full[acc], acc_phase, ctl, p.err);
+      if (lane == 0) ok = mbar_wait(&ctl->tmem_full[acc], acc_phase, &ctl->abort, p.err);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();

@@ -60,6 +60,7 @@ struct QkvArgs {
   float eps;
   int sec[3];             // 3D section widths (sum = d)
   int n_slots;            // rotation slots per head = d / 2
+  int nb;                 // depth of the shared-memory row ring (set by the launcher)
   // per slot: rotation frequency (hi + lo binary32 split of the float64 value),
   // which grid coordinate drives it, and its (lo, hi) element pair in the head
   float omega_hi[kMaxRopeSlots];

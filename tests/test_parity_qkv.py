@@ -81,6 +81,25 @@ def test_all_combinations(gbf, norm, rope, tokens, hq, hkv, d):
     check(gbf, c, f"norm {norm} rope {rope} [{tokens},{hq},{hkv},{d}]")
 
 
+@pytest.mark.parametrize("norm", [0, 1])
+@pytest.mark.parametrize("rope", [0, 1])
+def test_many_heads_two_pass_path(gbf, norm, rope):
+    """80 Q/K heads of width 256: more heads per thread than the single-pass
+    kernel keeps in registers, so the two-pass kernel runs."""
+    sections = (86, 86, 84) if rope else None
+    c = workloads.qkv_case(7, 64, 16, 256, norm, rope, seed=31 + norm + 2 * rope, theta=1e4,
+                           grid=(2, 2, 2) if rope else None, sections=sections)
+    check(gbf, c, f"two-pass norm {norm} rope {rope}")
+
+
+@pytest.mark.parametrize("rope", [0, 1])
+def test_full_width_head_dim_48(gbf, rope):
+    """Full-width norm with head_dim 48 (24 rotation slots, not a power of two)."""
+    c = workloads.qkv_case(9, 6, 2, 48, 1, rope, seed=41 + rope, theta=1e4, grid=(2, 3, 2) if rope else None,
+                           sections=(16, 16, 16) if rope else None)
+    check(gbf, c, f"head_dim 48 rope {rope}")
+
+
 def test_3d_per_head_with_zero_section(gbf):
     c = workloads.qkv_case(11, 4, 2, 128, 0, 1, seed=3, theta=1e4, grid=(2, 3, 4), sections=(64, 0, 64))
     check(gbf, c, "3D with an empty section")
