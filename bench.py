@@ -423,22 +423,21 @@ class ClockSampler:
 
 # ------------------------------------------------------------- traffic record
 
-def kernel_traffic(kernel_file, launches_per_op):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel's
-    source is unchanged since the counters were taken (else None)."""
+def kernel_traffic(op_name):
+    """DRAM bytes per launch of `op_name`'s kernel from the committed ncu record
+    (profiles/traffic.json), or None when the kernel's source has changed since
+    the counters were taken (or none were taken)."""
     rec = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "fusion_add_rmsnorm_gb300", "csrc", kernel_file)
-    if not (os.path.exists(rec) and os.path.exists(src)):
+    if not os.path.exists(rec):
         return None
     with open(rec) as f:
-        table = json.load(f)
-    ent = table.get(kernel_file)
+        ent = json.load(f).get("per_op", {}).get(op_name)
     if not ent:
         return None
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if ent.get("source_sha256_16") != h:
+    src = os.path.join(ROOT, "fusion_add_rmsnorm_gb300", "csrc", ent["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != ent["source_sha256_16"]:
         return None
-    return ent.get("dram_bytes_per_launch")
+    return ent["dram_bytes_per_launch"]
 
 
 KERNEL_FILE = {"add_rmsnorm_fp8": "add_rmsnorm_fp8.cu", "pi05_ada_chain": "add_rmsnorm_fp8.cu",
@@ -648,7 +647,7 @@ def main_gpu(args):
     roofline = {"kernel": dom_name, "bound": "hbm", "achieved": dom["gbs"], "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(dom["gbs"] / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peaks['source']} (burst copy)",
-                "traffic": kernel_traffic(KERNEL_FILE[dom_name], dom_op.launches),
+                "traffic": kernel_traffic(dom_name),
                 "algorithmic_bytes_per_launch": dom_op.algorithmic_bytes() // dom_op.launches}
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4), "higher_is_better": True,
@@ -667,7 +666,7 @@ def main_gpu(args):
                                  "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                  "frac": round(g["tflops"] / peaks["bf16_tflops"], 4),
                                  "peak_source": f"{peaks['source']} (burst cuBLAS bf16)",
-                                 "traffic": kernel_traffic("gemm_tcgen05.cu", 1)}
+                                 "traffic": kernel_traffic("linear_bias_gelu")}
 
     # end to end through the C ABI with host buffers: H2D inputs, op, D2H outputs
     if not args.no_e2e:

@@ -40,6 +40,7 @@ _SIGNATURES = {
     "gbf_bn_fold": [_p, _p, _p, _p, _p, _p, _f, _i64, _i64, _p, _p, _p],
     "gbf_copy": [_p, _p, _i64, _p],
     "gbf_device_status": [_p],
+    "gbf_selftest_bounded_wait": [_p],
     "gbf_last_error": [],
     "gbf_version": [],
 }
@@ -123,6 +124,11 @@ def copy(src, dst, nbytes=None, stream=None):
     """gbf_copy of nbytes (default: all of src) bytes."""
     n = src.numel() * src.element_size() if nbytes is None else nbytes
     return _check(_lib.gbf_copy(_ptr(src), _ptr(dst), n, _stream(stream)))
+
+
+def selftest_bounded_wait(stream=None):
+    """gbf_selftest_bounded_wait: enqueue the bounded-wait self-test kernel."""
+    return _check(_lib.gbf_selftest_bounded_wait(_stream(stream)))
 
 
 def device_status(stream=None):

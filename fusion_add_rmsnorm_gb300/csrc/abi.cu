@@ -308,6 +308,15 @@ GBF_API int gbf_copy(const void* src, void* dst, int64_t bytes, void* stream) {
   return launch_status(gbf::launch_copy(src, dst, bytes, static_cast<cudaStream_t>(stream)), fn);
 }
 
+// --------------------------------------------------- failure-path self-test
+
+GBF_API int gbf_selftest_bounded_wait(void* stream) {
+  unsigned int* err = error_word();
+  if (!err) return fail(GBF_ELAUNCH, "gbf_selftest_bounded_wait: no device error word (no CUDA device?)");
+  return launch_status(gbf::launch_bounded_wait_selftest(err, static_cast<cudaStream_t>(stream)),
+                       "gbf_selftest_bounded_wait");
+}
+
 // ----------------------------------------------------------- device status
 
 GBF_API int gbf_device_status(void* stream) {

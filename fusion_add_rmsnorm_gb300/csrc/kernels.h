@@ -92,6 +92,9 @@ cudaError_t launch_bn_fold(const BnFoldArgs& a, cudaStream_t stream);
 // ------------------------------------------------------------- copy probe
 cudaError_t launch_copy(const void* src, void* dst, int64_t bytes, cudaStream_t stream);
 
+// ------------------------------------------------------- failure self-test
+cudaError_t launch_bounded_wait_selftest(unsigned int* err, cudaStream_t stream);
+
 // ------------------------------------------------ Linear + bias + GELU GEMM
 struct GemmArgs {
   const void* x;          // [M, K] bf16, K-major

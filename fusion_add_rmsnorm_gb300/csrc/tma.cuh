@@ -6,7 +6,8 @@
 
 namespace gbf {
 
-constexpr uint64_t kWaitBudgetNs = 1000000000ull;   // a bounded wait gives up after ~1 s
+constexpr uint64_t kWaitBudgetNs = 1000000000ull;   // a bounded wait gives up after ~1 s ...
+constexpr uint32_t kWaitMaxPolls = 1u << 23;         // ... or after this many polls (~2 s of backoff)
 
 GBF_DEVICE uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -44,7 +45,9 @@ GBF_DEVICE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase of `bar` with parity `parity` to complete.
-// Gives up after kWaitBudgetNs, or as soon as *abort is set by another thread;
+// Gives up after kWaitBudgetNs or kWaitMaxPolls polls (whichever comes first,
+// so the wait ends even if the timer were to stall), or as soon as *abort is
+// set by another thread;
 // a thread that gives up on its own sets *abort and the device error bit.
 GBF_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, int* abort, unsigned int* err) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -60,7 +63,7 @@ GBF_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, int* abort, unsigned i
     }
     if ((i & 15u) == 0) {
       if (*reinterpret_cast<volatile int*>(abort)) return false;
-      if (global_timer() - t0 > kWaitBudgetNs) {
+      if (global_timer() - t0 > kWaitBudgetNs || i >= kWaitMaxPolls) {
         raise_error(err, DEV_ERR_MBAR_TIMEOUT);
         *reinterpret_cast<volatile int*>(abort) = 1;
         return false;

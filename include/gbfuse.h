@@ -179,6 +179,16 @@ GBF_API int gbf_copy(const void* src, void* dst, int64_t bytes, void* stream);
  */
 GBF_API int gbf_device_status(void* stream);
 
+/*
+ * gbf_selftest_bounded_wait -- exercises the device-side failure path: a
+ * one-thread kernel waits, through the same bounded mbarrier wait the
+ * pipelined kernels use, on a barrier nothing arrives at.  After about one
+ * second the wait gives up, sets the timeout bit of the device error word and
+ * the kernel returns normally; the next gbf_device_status(stream) returns
+ * GBF_ETIMEOUT and the context stays usable.  Enqueues asynchronously.
+ */
+GBF_API int gbf_selftest_bounded_wait(void* stream);
+
 /* Message for the calling thread's most recent non-OK return ("" if none). */
 GBF_API const char* gbf_last_error(void);
 

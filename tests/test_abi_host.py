@@ -28,7 +28,7 @@ def gbf():
 def test_header_declares_the_entry_points():
     assert declared_symbols() == sorted(["gbf_add_rmsnorm_fp8", "gbf_qkv_split_norm_rope", "gbf_linear_bias_gelu",
                                          "gbf_bn_fold", "gbf_copy", "gbf_device_status", "gbf_last_error",
-                                         "gbf_version"])
+                                         "gbf_version", "gbf_selftest_bounded_wait"])
 
 
 def test_library_exports_every_declared_symbol(gbf):
