@@ -150,6 +150,10 @@ GBF_API int gbf_qkv_split_norm_rope(const void* qkv, int64_t tokens, int n_q_hea
   if (norm == GBF_QKNORM_PER_HEAD && (head_dim & (head_dim - 1)) != 0)
     return fail(GBF_EUNSUPPORTED, "%s: per-head norm needs a power-of-two head_dim (got %d)", fn, head_dim);
   if (n_q_heads > 4096 || n_kv_heads > 4096) return fail(GBF_EUNSUPPORTED, "%s: too many heads", fn);
+  if (!gbf::qkv_uses_rot1d(norm, rope, head_dim) &&
+      (6LL * n_q_heads + 8LL * n_kv_heads) * head_dim > gbf::kQkvStagedMaxBytes)
+    return fail(GBF_EUNSUPPORTED, "%s: (6 n_q_heads + 8 n_kv_heads) * head_dim must be <= %lld for this norm/rope",
+                fn, (long long)gbf::kQkvStagedMaxBytes);
   int sec[3] = {head_dim, 0, 0};
   if (rope == GBF_ROPE_3D) {
     if (!sections) return fail(GBF_EINVAL, "%s: 3D RoPE needs sections[3]", fn);

@@ -11,6 +11,7 @@
 #include <stdint.h>
 
 #define GBF_DEVICE __device__ __forceinline__
+#define GBF_HOST_DEVICE __host__ __device__ __forceinline__
 
 namespace gbf {
 
@@ -71,6 +72,30 @@ GBF_DEVICE uint4 f32x8_to_bf16x8(const float f[8]) {
 }
 
 GBF_DEVICE float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+// a * b + c for bf16 a, b (the halves `lo`/`hi` of packed words) and float32
+// c, rounded once to float32.  A bf16 x bf16 product is exact in float32, so
+// with c = 0 this is the float32 product of the widened values.
+GBF_DEVICE float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %1;\n\t"
+      "mov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+GBF_DEVICE float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %1;\n\t"
+      "mov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
 
 // --------------------------------------------------------------- E4M3 packing
 

@@ -60,7 +60,9 @@ struct QkvArgs {
   float eps;
   int sec[3];             // 3D section widths (sum = d)
   int n_slots;            // rotation slots per head = d / 2
-  int nb;                 // depth of the shared-memory row ring (set by the launcher)
+  // staged kernel, set by the launcher: worker threads per CTA, bank swizzle
+  // bit, depth of the shared-memory row ring
+  int active, swz2, nb;
   // per slot: rotation frequency (hi + lo binary32 split of the float64 value),
   // which grid coordinate drives it, and its (lo, hi) element pair in the head
   float omega_hi[kMaxRopeSlots];
@@ -71,6 +73,11 @@ struct QkvArgs {
 };
 
 cudaError_t launch_qkv_split_norm_rope(const QkvArgs& a, cudaStream_t stream);
+// True when the register-only per-head 1D kernel handles (norm, rope, d).  Every
+// other case stages a token's packed row (bf16) and its Q and K (float32) in
+// shared memory, which bounds (6 n_q + 8 n_kv) * d by kQkvStagedMaxBytes.
+bool qkv_uses_rot1d(int norm, int rope, int d);
+constexpr int64_t kQkvStagedMaxBytes = 196608;
 
 // ------------------------------------------------------------ BN folding
 struct BnFoldArgs {

@@ -26,8 +26,7 @@
 // [-pi, pi] is below 2^-21.4.  The angle error stays near 1e-7 rad at
 // position 4095, where a plain binary32 product would be 2.4e-4 rad off.
 //
-// Two kernels, both streaming (outputs leave from registers, no persistent
-// state):
+// Two kernels:
 //  * qkv_rot1d_kernel (per-head norm, 1D, head_dim 64/128/256): D/16 lanes
 //    own a head; lane l holds the 16-byte vectors l and l + D/16, which contain
 //    both members of its 8 rotation pairs (j, j + D/2), so the rotation is done
@@ -35,17 +34,20 @@
 //    head's lanes.  Each thread visits every 8th head of its token (V heads are
 //    copied), issuing a batch of loads before any arithmetic, and computes the
 //    (cos, sin) of its 8 slots once per token.
-//  * qkv_staged_kernel (everything else: full-width norm and/or 3D sections):
-//    one CTA per token loads the packed row with 16-byte vectors, writes V
-//    straight back out, stages the raw bf16 Q and K in shared memory while the
-//    sums of squares are reduced, and after one barrier each thread - owning one
-//    rotation slot - weights, rotates and scales that slot's pair in every head
-//    it visits and stores both outputs directly.
+//  * qkv_staged_kernel (everything else: full-width norm and/or 3D sections,
+//    where a rotation pair need not sit in one 16-byte vector): a persistent
+//    CTA streams its tokens' packed rows through a ring of shared-memory
+//    buffers filled by bulk copies.  Per token, phase 1 copies V out and writes
+//    x * w of Q and K to shared memory as float32 while the sums of squares
+//    are reduced; after one barrier each thread takes its own 16-byte vectors
+//    again, reads the 8 rotation partners of their elements, and stores the
+//    rotated, normalised vector with one 16-byte store.
 #include <map>
 #include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tma.cuh"
 
 namespace gbf {
 namespace {
@@ -183,119 +185,338 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
 }
 
 // ------------------------------------------------------------- staged path
+//
+// A CTA handles the tokens blockIdx.x, blockIdx.x + gridDim.x, ...  Thread 0
+// keeps a ring of `nb` shared-memory row buffers filled with bulk copies of the
+// packed rows of the CTA's next tokens (completion counted on one mbarrier per
+// buffer), so the row of the next token is in flight while the current one is
+// computed.  Worker thread tid < active owns the 16-byte vectors
+// v = tid + k * active of the row.  active is a multiple of head_dim / 8, so all
+// of a thread's vectors sit at the same position P0 = 8 * (tid % (head_dim / 8))
+// inside their heads: the thread's rotation partners, (cos, sin) values and
+// shared-memory offsets are fixed for the whole token.
 
-constexpr int kStagedMaxBlock = 256;
+constexpr int kStagedBlock = 256;
 constexpr int kStagedUnroll = 4;
+constexpr uint32_t kBulkChunk = 32768;      // bytes per bulk copy instruction
 
-template <bool FULL>
-__global__ void __launch_bounds__(kStagedMaxBlock, 4)
-qkv_staged_kernel(const __grid_constant__ QkvArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int D = a.d;
-  const int n_slots = a.n_slots;
-  const int nqk = a.n_q + a.n_kv;
-  const int vph = D >> 3;
-  const int qk_vec = nqk * vph;
-  const int all_vec = (nqk + a.n_kv) * vph;
-  const int nthreads = blockDim.x;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
-  __nv_bfloat16* raw = reinterpret_cast<__nv_bfloat16*>(smem);                            // [nqk * D]
-  SlotEntry* tab = reinterpret_cast<SlotEntry*>(smem + ((nqk * D * 2 + 15) & ~15));      // [n_slots]
-  float* inv_head = reinterpret_cast<float*>(tab + n_slots);                              // [nqk]
-  float* red = inv_head + nqk;                                                            // [2 * warps]
+// Word offset in shared memory of element L of a token's staged Q|K block.  The
+// two 16-byte halves of vector L / 8 trade places when bit 2 (and, if swz2 is
+// set, bit 4) of the vector index is odd, which spreads a quarter warp's
+// 16-byte accesses and the warp's partner reads over the 32 banks.
+GBF_DEVICE int staged_word(int L, int swz2) {
+  const int v = L >> 3;
+  const int s = ((v >> 2) ^ ((v >> 4) & swz2)) & 1;
+  return L ^ (s << 2);
+}
 
-  stage_slot_table(a, tab);
-  const int64_t t = blockIdx.x;
-  bool slot_ok;
-  const int64_t crow = cache_slot(a, t, slot_ok);
-  if (!slot_ok && tid == 0) raise_error(a.err, DEV_ERR_SLOT_RANGE);
+// Index in the (cos, sin) table of head position P: the pairs of positions
+// 8g + 2i and 8g + 2i + 1 share the float4 i * vph + g, so the lanes that own
+// consecutive 8-element groups g read consecutive float4s.
+GBF_DEVICE int cs_slot(int P, int vph) { return 2 * (((P & 7) >> 1) * vph + (P >> 3)) + (P & 1); }
 
-  // Phase 1: stream the row; V goes straight out, raw Q/K to shared memory.
-  const __nv_bfloat16* row = static_cast<const __nv_bfloat16*>(a.qkv) + t * static_cast<int64_t>(all_vec) * 8;
-  float ss_q = 0.f, ss_k = 0.f;
-  for (int base = 0; base < all_vec; base += kStagedUnroll * nthreads) {
-    uint4 val[kStagedUnroll];
-#pragma unroll
-    for (int k = 0; k < kStagedUnroll; ++k) {
-      const int v = base + k * nthreads + tid;
-      if (v < all_vec) val[k] = ld_stream(row + v * 8);
-    }
-#pragma unroll
-    for (int k = 0; k < kStagedUnroll; ++k) {
-      const int v = base + k * nthreads + tid;
-      float part = 0.f;
-      if (v < qk_vec) {
-        *reinterpret_cast<uint4*>(raw + v * 8) = val[k];
-        float x[8];
-        bf16x8_to_f32(val[k], x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) part = fmaf(x[i], x[i], part);
-        if (FULL) {
-          if (v < a.n_q * vph) ss_q += part; else ss_k += part;
-        }
-      } else if (v < all_vec && slot_ok) {
-        st_16(static_cast<__nv_bfloat16*>(a.v_cache) + crow * a.n_kv * D + (v - qk_vec) * 8, val[k]);
-      }
-      if (!FULL) {
-        // vph consecutive lanes hold one head in this trip (the block is a multiple of vph)
-        const float hs = group_sum(part, vph);
-        if (v < qk_vec && (tid & (vph - 1)) == 0)
-          inv_head[v / vph] = 1.0f / sqrtf(hs / static_cast<float>(D) + a.eps);
-      }
-    }
-  }
-  if (FULL) {
-    ss_q = warp_sum(ss_q);
-    ss_k = warp_sum(ss_k);
-    if (lane == 0) {
-      red[2 * warp] = ss_q;
-      red[2 * warp + 1] = ss_k;
-    }
-  }
-  __syncthreads();
-  float inv_q = 0.f, inv_k = 0.f;
-  if (FULL) {                                   // each warp reduces the warps' partials
-    float sq = lane < nwarps ? red[2 * lane] : 0.f;
-    float sk = lane < nwarps ? red[2 * lane + 1] : 0.f;
-    sq = warp_sum(sq);
-    sk = warp_sum(sk);
-    inv_q = 1.0f / sqrtf(sq / static_cast<float>(a.n_q * D) + a.eps);
-    inv_k = 1.0f / sqrtf(sk / static_cast<float>(a.n_kv * D) + a.eps);
-  }
-
-  // Phase 2: this thread's slot in every head it visits.
-  const int p = tid % n_slots;
-  const int grp = tid / n_slots;
-  const int ngrp = nthreads / n_slots;
-  const SlotEntry e = tab[p];
-  const int lo = e.lo, hi = e.hi_axis & 0xFFFF, axis = e.hi_axis >> 16;
-  const int pos = a.rope == kRope3D ? a.pos[t * 3 + axis] : a.pos[t];
-  const float2 c = rope_cos_sin(pos, e.om_hi, e.om_lo);
-  const uint16_t* qw = static_cast<const uint16_t*>(a.q_w);
-  const uint16_t* kw = static_cast<const uint16_t*>(a.k_w);
-  __nv_bfloat16* q_out = static_cast<__nv_bfloat16*>(a.q_out) + t * a.n_q * D;
-  __nv_bfloat16* k_out = static_cast<__nv_bfloat16*>(a.k_cache) + crow * a.n_kv * D;
-  for (int h = grp; h < nqk; h += ngrp) {
-    const bool is_q = h < a.n_q;
-    const int hl = is_q ? h : h - a.n_q;
-    if (!is_q && !slot_ok) continue;
-    const uint16_t* w = (is_q ? qw : kw) + (FULL ? hl * D : 0);
-    const float xl = __bfloat162float(raw[h * D + lo]);
-    const float xh = __bfloat162float(raw[h * D + hi]);
-    const float ul = xl * bf16_bits_to_f32(w[lo]);
-    const float uh = xh * bf16_bits_to_f32(w[hi]);
-    const float inv = FULL ? (is_q ? inv_q : inv_k) : inv_head[h];
-    __nv_bfloat16* dst = (is_q ? q_out : k_out) + hl * D;
-    dst[lo] = __float2bfloat16_rn((ul * c.x - uh * c.y) * inv);
-    dst[hi] = __float2bfloat16_rn((uh * c.x + ul * c.y) * inv);
+// Thread 0: copy one packed row into a ring buffer, completion on `bar`.
+GBF_DEVICE void load_row(uint8_t* dst, const uint8_t* src, uint32_t bytes, uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, bytes);
+  for (uint32_t o = 0; o < bytes; o += kBulkChunk) {
+    const uint32_t n = bytes - o < kBulkChunk ? bytes - o : kBulkChunk;
+    bulk_load(dst + o, src + o, n, bar);
   }
 }
 
-size_t staged_smem_bytes(const QkvArgs& a, int threads) {
-  const size_t nqk = static_cast<size_t>(a.n_q + a.n_kv);
-  return ((nqk * a.d * 2 + 15) & ~size_t(15)) + a.n_slots * sizeof(SlotEntry) + nqk * sizeof(float) +
-         2 * (threads / 32) * sizeof(float);
+struct StagedLayout {
+  size_t raw_stride, u_off, tab_off, cs_off, part_off, inv_off, red_off, bar_off, total;
+};
+
+GBF_HOST_DEVICE StagedLayout staged_layout(int n_q, int n_kv, int d, int n_slots, int nwarps, int nb) {
+  StagedLayout L;
+  const size_t nqk = static_cast<size_t>(n_q + n_kv);
+  const size_t row = (nqk + n_kv) * d * 2;
+  L.raw_stride = (row + 127) & ~size_t(127);
+  L.u_off = nb * L.raw_stride;
+  L.tab_off = L.u_off + nqk * d * sizeof(float);
+  L.cs_off = L.tab_off + n_slots * sizeof(SlotEntry);
+  L.part_off = L.cs_off + d * sizeof(float2);
+  L.inv_off = L.part_off + d * sizeof(int);
+  L.red_off = L.inv_off + nqk * sizeof(float);
+  L.bar_off = (L.red_off + 2 * nwarps * sizeof(float) + 7) & ~size_t(7);
+  L.total = L.bar_off + nb * sizeof(uint64_t) + sizeof(int);
+  return L;
+}
+
+// Phase 1 work on one Q|K vector v: x * w to shared memory (float32), the
+// sum of squares to ss_q / ss_k (full width) or, per head, the head's inverse
+// RMS to inv_head (the head's vph lanes run this together).
+template <bool FULL>
+GBF_DEVICE void stage_vector(const QkvArgs& a, int v, uint4 xv, uint4 wv, uint32_t u_dst, int own_lo_b,
+                             int own_hi_b, int q_vec, int vph, int lg_vph, float* inv_head, float& ss_q,
+                             float& ss_k) {
+  const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+  const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+  float xw[8], p0 = 0.f, p1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    xw[2 * i] = fma_bf16_lo(xs[i], ws[i], 0.f);
+    xw[2 * i + 1] = fma_bf16_hi(xs[i], ws[i], 0.f);
+    p0 = fma_bf16_lo(xs[i], xs[i], p0);
+    p1 = fma_bf16_hi(xs[i], xs[i], p1);
+  }
+  sts128f(u_dst + own_lo_b, xw[0], xw[1], xw[2], xw[3]);
+  sts128f(u_dst + own_hi_b, xw[4], xw[5], xw[6], xw[7]);
+  const float part = p0 + p1;
+  if (FULL) {
+    if (v < q_vec) ss_q += part; else ss_k += part;
+  } else {
+    const float hs = segment_sum(part, vph);
+    if ((threadIdx.x & (vph - 1)) == 0) inv_head[v >> lg_vph] = 1.0f / sqrtf(hs / static_cast<float>(a.d) + a.eps);
+  }
+}
+
+// Phase 2 work on one Q|K vector: rotate, normalise, one 16-byte store.
+template <bool FULL>
+GBF_DEVICE void rotate_vector(int v, float4 o0, float4 o1, const float pv[8], const float2 c2[4],
+                              const float2 s2[4], float inv, __nv_bfloat16* q_dst, __nv_bfloat16* k_dst, int q_vec,
+                              bool slot_ok) {
+  const float2 own[4] = {make_float2(o0.x, o0.y), make_float2(o0.z, o0.w), make_float2(o1.x, o1.y),
+                         make_float2(o1.z, o1.w)};
+  const float2 inv2 = make_float2(inv, inv);
+  uint32_t packed[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 p2 = make_float2(pv[2 * i], pv[2 * i + 1]);
+    const float2 o = __fmul2_rn(__ffma2_rn(own[i], c2[i], __fmul2_rn(s2[i], p2)), inv2);
+    packed[i] = f32x2_to_bf16x2(o.x, o.y);
+  }
+  const uint4 o16 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  if (v < q_vec)
+    st_16(q_dst + v * 8, o16);
+  else if (slot_ok)
+    st_16(k_dst + (v - q_vec) * 8, o16);
+}
+
+template <bool FULL>
+__global__ void __launch_bounds__(kStagedBlock, 2)
+qkv_staged_kernel(const __grid_constant__ QkvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int D = a.d;
+  const int vph = D >> 3;
+  const int n_slots = a.n_slots;
+  const int nqk = a.n_q + a.n_kv;
+  const int q_vec = a.n_q * vph;
+  const int qk_vec = nqk * vph;
+  const int all_vec = (nqk + a.n_kv) * vph;
+  const int active = a.active;
+  const int swz2 = a.swz2;
+  const int nb = a.nb;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const bool worker = tid < active;
+  const StagedLayout L = staged_layout(a.n_q, a.n_kv, D, n_slots, nwarps, nb);
+  const uint32_t row_bytes = static_cast<uint32_t>(all_vec) * 16u;
+  const uint32_t smem32 = smem_u32(smem);
+  const uint32_t u32 = smem32 + static_cast<uint32_t>(L.u_off);          // [qk_vec * 8] x * w
+  SlotEntry* tab = reinterpret_cast<SlotEntry*>(smem + L.tab_off);        // [n_slots]
+  float2* cs_pos = reinterpret_cast<float2*>(smem + L.cs_off);            // [D] (cos, -+sin), cs_slot order
+  int* part_pos = reinterpret_cast<int*>(smem + L.part_off);              // [D] rotation partner
+  float* inv_head = reinterpret_cast<float*>(smem + L.inv_off);           // [nqk]
+  float* red = reinterpret_cast<float*>(smem + L.red_off);                // [2 * warps]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);         // [nb]
+  int* abort_flag = reinterpret_cast<int*>(full + nb);
+  const uint8_t* qkv = static_cast<const uint8_t*>(a.qkv);
+
+  for (int p = tid; p < n_slots; p += blockDim.x) {
+    SlotEntry e;
+    e.om_hi = a.omega_hi[p];
+    e.om_lo = a.omega_lo[p];
+    e.lo = a.lo_idx[p];
+    e.hi_axis = a.hi_idx[p] | (a.axis[p] << 16);
+    tab[p] = e;
+    part_pos[a.lo_idx[p]] = a.hi_idx[p];
+    part_pos[a.hi_idx[p]] = a.lo_idx[p];
+  }
+  if (tid == 0) {
+    for (int b = 0; b < nb; ++b) mbar_init(&full[b], 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int b = 0; b < nb; ++b) {
+      const int64_t tb = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
+      if (tb < a.tokens) load_row(smem + b * L.raw_stride, qkv + tb * row_bytes, row_bytes, &full[b]);
+    }
+  }
+
+  const int P0 = worker ? 8 * (tid % vph) : 0;
+  const int lg_vph = __ffs(vph) - 1;          // per-head norm: vph is a power of two
+  // Byte offsets, from the start of vector v in `u`, of the thread's own
+  // halves and of its 8 partners; the same for every v = tid + k * active.
+  const int vref = tid + 64 * active;
+  const int own_lo_b = 4 * (staged_word(8 * vref, swz2) - 8 * vref);
+  const int own_hi_b = 16 - own_lo_b;
+  int off_b[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) off_b[e] = 4 * (staged_word(8 * vref + part_pos[P0 + e] - P0, swz2) - 8 * vref);
+
+  const __nv_bfloat16* qw = static_cast<const __nv_bfloat16*>(a.q_w);
+  const __nv_bfloat16* kw = static_cast<const __nv_bfloat16*>(a.k_w);
+  // weight vector of Q|K vector v
+  auto wptr = [&](int v) -> const __nv_bfloat16* {
+    return FULL ? (v < q_vec ? qw + v * 8 : kw + (v - q_vec) * 8) : (v < q_vec ? qw : kw) + P0;
+  };
+  int b = 0;                      // ring buffer of the current token
+  uint32_t phase_bits = 0;        // bit j: parity of the next completion of buffer j
+  for (int64_t t = blockIdx.x; t < a.tokens; t += gridDim.x) {
+    const uint32_t raw32 = smem32 + static_cast<uint32_t>(b * L.raw_stride);
+    bool slot_ok;
+    const int64_t crow = cache_slot(a, t, slot_ok);
+    if (!slot_ok && tid == 0) raise_error(a.err, DEV_ERR_SLOT_RANGE);
+    for (int p = tid; p < n_slots; p += blockDim.x) {
+      const SlotEntry e = tab[p];
+      const int pos = a.rope == kRope3D ? a.pos[t * 3 + (e.hi_axis >> 16)] : a.pos[t];
+      const float2 cs = rope_cos_sin(pos, e.om_hi, e.om_lo);
+      cs_pos[cs_slot(e.lo, vph)] = make_float2(cs.x, -cs.y);
+      cs_pos[cs_slot(e.hi_axis & 0xFFFF, vph)] = cs;
+    }
+
+    // Phase 1: x * w of Q/K to `u`, V from the ring buffer straight out.
+    const bool ok = mbar_wait_warp(&full[b], (phase_bits >> b) & 1u, abort_flag, a.err);
+    float ss_q = 0.f, ss_k = 0.f;
+    if (ok && worker) {
+      int v = tid;
+      for (; v + (kStagedUnroll - 1) * active < qk_vec; v += kStagedUnroll * active) {
+        uint4 xv[kStagedUnroll], wv[kStagedUnroll];
+#pragma unroll
+        for (int k = 0; k < kStagedUnroll; ++k) {
+          xv[k] = lds128(raw32 + (v + k * active) * 16);
+          wv[k] = ld_cached(wptr(v + k * active));
+        }
+#pragma unroll
+        for (int k = 0; k < kStagedUnroll; ++k) {
+          const int vk = v + k * active;
+          stage_vector<FULL>(a, vk, xv[k], wv[k], u32 + vk * 32, own_lo_b, own_hi_b, q_vec, vph, lg_vph, inv_head,
+                             ss_q, ss_k);
+        }
+      }
+      for (; v < qk_vec; v += active)
+        stage_vector<FULL>(a, v, lds128(raw32 + v * 16), ld_cached(wptr(v)), u32 + v * 32, own_lo_b, own_hi_b, q_vec,
+                           vph, lg_vph, inv_head, ss_q, ss_k);
+      if (slot_ok) {
+        __nv_bfloat16* v_dst =
+            static_cast<__nv_bfloat16*>(a.v_cache) + crow * a.n_kv * D - static_cast<int64_t>(qk_vec) * 8;
+        int w = qk_vec + tid;
+        for (; w + (kStagedUnroll - 1) * active < all_vec; w += kStagedUnroll * active) {
+          uint4 xv[kStagedUnroll];
+#pragma unroll
+          for (int k = 0; k < kStagedUnroll; ++k) xv[k] = lds128(raw32 + (w + k * active) * 16);
+#pragma unroll
+          for (int k = 0; k < kStagedUnroll; ++k) st_16(v_dst + (w + k * active) * 8, xv[k]);
+        }
+        for (; w < all_vec; w += active) st_16(v_dst + w * 8, lds128(raw32 + w * 16));
+      }
+    }
+    if (FULL) {
+      ss_q = warp_sum(ss_q);
+      ss_k = warp_sum(ss_k);
+      if (lane == 0) {
+        red[2 * warp] = ss_q;
+        red[2 * warp + 1] = ss_k;
+      }
+    }
+    if (__syncthreads_or(!ok)) {
+      // A row never arrived: wait (bounded) for the copies still in flight, then leave.
+      if (tid == 0) {
+        int give_up = 0;
+        for (int j = 0, bj = b; j < nb; ++j, bj = bj + 1 == nb ? 0 : bj + 1) {
+          if (t + static_cast<int64_t>(j) * gridDim.x >= a.tokens) break;
+          mbar_wait(&full[bj], (phase_bits >> bj) & 1u, &give_up, a.err);
+        }
+      }
+      return;
+    }
+    // The row buffer is consumed: refill it with the token nb turns ahead.
+    if (tid == 0) {
+      const int64_t tn = t + static_cast<int64_t>(nb) * gridDim.x;
+      if (tn < a.tokens) {
+        fence_proxy_async_smem();   // the barrier ordered every thread's reads of the buffer before this
+        load_row(smem + b * L.raw_stride, qkv + tn * row_bytes, row_bytes, &full[b]);
+      }
+    }
+    phase_bits ^= 1u << b;
+    b = b + 1 == nb ? 0 : b + 1;
+
+    // Phase 2: o = (u * cos -+ u_partner * sin) * inv, 16-byte stores from registers.
+    float inv_q = 0.f, inv_k = 0.f;
+    if (FULL) {                                  // every warp reduces the warps' partials
+      float sq = lane < nwarps ? red[2 * lane] : 0.f;
+      float sk = lane < nwarps ? red[2 * lane + 1] : 0.f;
+      sq = warp_sum(sq);
+      sk = warp_sum(sk);
+      inv_q = 1.0f / sqrtf(sq / static_cast<float>(a.n_q * D) + a.eps);
+      inv_k = 1.0f / sqrtf(sk / static_cast<float>(a.n_kv * D) + a.eps);
+    }
+    if (worker) {
+      float2 c2[4], s2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 q = reinterpret_cast<const float4*>(cs_pos)[i * vph + (P0 >> 3)];
+        c2[i] = make_float2(q.x, q.z);
+        s2[i] = make_float2(q.y, q.w);
+      }
+      __nv_bfloat16* q_dst = static_cast<__nv_bfloat16*>(a.q_out) + t * a.n_q * D;
+      __nv_bfloat16* k_dst = static_cast<__nv_bfloat16*>(a.k_cache) + crow * a.n_kv * D;
+      auto inv_of = [&](int v) { return FULL ? (v < q_vec ? inv_q : inv_k) : inv_head[v >> lg_vph]; };
+      int v = tid;
+      for (; v + active < qk_vec; v += 2 * active) {
+        float4 o[2][2];
+        float pv[2][8];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t a0 = u32 + (v + k * active) * 32;
+          o[k][0] = lds128f(a0 + own_lo_b);
+          o[k][1] = lds128f(a0 + own_hi_b);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) pv[k][e] = lds32f(a0 + off_b[e]);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          rotate_vector<FULL>(v + k * active, o[k][0], o[k][1], pv[k], c2, s2, inv_of(v + k * active), q_dst, k_dst,
+                              q_vec, slot_ok);
+      }
+      if (v < qk_vec) {
+        const uint32_t a0 = u32 + v * 32;
+        float pv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) pv[e] = lds32f(a0 + off_b[e]);
+        rotate_vector<FULL>(v, lds128f(a0 + own_lo_b), lds128f(a0 + own_hi_b), pv, c2, s2, inv_of(v), q_dst, k_dst,
+                            q_vec, slot_ok);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+int gcd_int(int x, int y) {
+  while (y) {
+    const int r = x % y;
+    x = y;
+    y = r;
+  }
+  return x;
+}
+
+// Worker threads per CTA: a multiple of lcm(vph, 32) (both swizzle bits) or
+// else of lcm(vph, 8) (bit 2 only), at most kStagedBlock.
+void staged_shape(const QkvArgs& a, int& active, int& swz2) {
+  const int vph = a.d / 8;
+  const int l32 = vph / gcd_int(vph, 32) * 32;
+  if (l32 <= kStagedBlock) {
+    active = kStagedBlock / l32 * l32;
+    swz2 = 1;
+  } else {
+    const int l8 = vph / gcd_int(vph, 8) * 8;
+    active = kStagedBlock / l8 * l8;
+    swz2 = 0;
+  }
 }
 
 // The dynamic shared memory limit of `fn` is raised once to the device's
@@ -315,11 +536,43 @@ cudaError_t raise_smem_limit(F fn) {
   return e;
 }
 
+template <bool FULL>
+cudaError_t launch_staged(const QkvArgs& a, cudaStream_t stream) {
+  QkvArgs b = a;
+  staged_shape(a, b.active, b.swz2);
+  const int threads = (b.active + 31) & ~31;
+  int dev = 0, sms = 0, optin = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  // two ring buffers when they fit, else one (no overlap inside the CTA)
+  b.nb = 2;
+  size_t smem = staged_layout(b.n_q, b.n_kv, b.d, b.n_slots, threads / 32, b.nb).total;
+  if (smem > static_cast<size_t>(optin)) {
+    b.nb = 1;
+    smem = staged_layout(b.n_q, b.n_kv, b.d, b.n_slots, threads / 32, b.nb).total;
+    if (smem > static_cast<size_t>(optin)) return cudaErrorInvalidValue;
+  }
+  cudaError_t e = raise_smem_limit(qkv_staged_kernel<FULL>);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qkv_staged_kernel<FULL>, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidValue;
+  const int64_t resident = static_cast<int64_t>(sms) * per_sm;
+  const unsigned grid = static_cast<unsigned>(a.tokens < resident ? a.tokens : resident);
+  qkv_staged_kernel<FULL><<<grid, threads, smem, stream>>>(b);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+bool qkv_uses_rot1d(int norm, int rope, int d) {
+  return norm == kQkNormPerHead && rope == kRope1D && (d == 64 || d == 128 || d == 256);
+}
 
 cudaError_t launch_qkv_split_norm_rope(const QkvArgs& a, cudaStream_t stream) {
   if (a.tokens == 0) return cudaSuccess;
-  if (a.norm == kQkNormPerHead && a.rope == kRope1D && (a.d == 64 || a.d == 128 || a.d == 256)) {
+  if (qkv_uses_rot1d(a.norm, a.rope, a.d)) {
     const int lph = a.d / 16;
     const int tok_per_cta = kRotBlock / (kRotGroups * lph);
     const unsigned grid = static_cast<unsigned>((a.tokens + tok_per_cta - 1) / tok_per_cta);
@@ -330,21 +583,7 @@ cudaError_t launch_qkv_split_norm_rope(const QkvArgs& a, cudaStream_t stream) {
     }
     return cudaGetLastError();
   }
-  // Block: the largest multiple of lcm(D/2, 32) that is <= kStagedMaxBlock.
-  int l = a.n_slots;
-  while (l % 32) l += a.n_slots;
-  const int threads = (kStagedMaxBlock / l) * l;
-  if (threads < 32) return cudaErrorInvalidConfiguration;
-  const size_t smem = staged_smem_bytes(a, threads);
-  if (smem > 200 * 1024) return cudaErrorInvalidValue;
-  const bool full = a.norm == kQkNormFullWidth;
-  cudaError_t e = full ? raise_smem_limit(qkv_staged_kernel<true>) : raise_smem_limit(qkv_staged_kernel<false>);
-  if (e != cudaSuccess) return e;
-  if (full)
-    qkv_staged_kernel<true><<<static_cast<unsigned>(a.tokens), threads, smem, stream>>>(a);
-  else
-    qkv_staged_kernel<false><<<static_cast<unsigned>(a.tokens), threads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return a.norm == kQkNormFullWidth ? launch_staged<true>(a, stream) : launch_staged<false>(a, stream);
 }
 
 }  // namespace gbf

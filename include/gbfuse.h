@@ -116,6 +116,11 @@ GBF_API int gbf_add_rmsnorm_fp8(const void* x, const void* res_in, void* res_out
  *   [0, cache_rows) skips that token's K/V writes and sets the device error word.
  * Requires head_dim % 16 == 0 and head_dim <= 256; per-head norm needs a
  * power-of-two head_dim; 16-byte aligned tensors; eps >= 0; theta > 0.
+ * Unless norm is per head, rope is 1D and head_dim is 64, 128 or 256, a token's
+ * row is staged on chip and (6 n_q_heads + 8 n_kv_heads) * head_dim must be
+ * <= 196608 (GBF_EUNSUPPORTED otherwise).  The staged kernel's waits for its
+ * row copies are bounded: a wait that gives up sets the device error word
+ * (gbf_device_status() returns GBF_ETIMEOUT) and the outputs are undefined.
  * Outputs may not overlap each other or the inputs (GBF_EINVAL).
  */
 GBF_API int gbf_qkv_split_norm_rope(const void* qkv, int64_t tokens, int n_q_heads, int n_kv_heads,
