@@ -15,8 +15,9 @@ own seeded synthetic inputs already resident in HBM:
   bn_fold              W [16384, 4096], BN of its 16384 output channels
 
 Timing: every operator is bracketed by CUDA events on the stream it is
-launched on; L2 (129 MB) is flushed by writing a 512 MB buffer before each
-operator, outside the event pair.  K steps are timed after W warm-up steps,
+launched on; L2 (129 MB) is flushed before each operator, outside the event
+pair, by writing a 512 MB buffer and then reading it back, so the operator
+starts with a cold L2 that holds no dirty lines of the flush to write back.  K steps are timed after W warm-up steps,
 with a barrier and a device synchronisation on both sides; the slowest rank
 counts.  `value` is the aggregate HBM throughput of the memory-bound fused
 kernels: their algorithmic bytes summed over the step divided by their summed
@@ -575,12 +576,17 @@ def main_gpu(args):
     with_gemm = not args.no_gemm
     ops = build_ops(gbf, with_gemm, args.only.split(",") if args.only else None, args.small)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_words = flush.view(torch.int64)
+
+    def flush_l2():
+        flush.fill_(1)               # evicts everything the last operator left in L2 ...
+        flush_words.sum()            # ... and the read-back leaves only clean lines behind
     stream = torch.cuda.current_stream()
 
     def one_step(record):
         times = {}
         for op in ops:
-            flush.fill_(1)
+            flush_l2()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             op.run()
@@ -654,7 +660,7 @@ def main_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp32 math, bf16/e4m3 out",
             "data": "synthetic (seeded numpy PCG64, the workloads' shapes and distributions)",
             "config": {"workload": "fused hot path: " + ", ".join(per_op), "parallelism": f"replicas x{world}",
-                       "l2": "flushed (512 MB write) before every operator, outside its event pair",
+                       "l2": "flushed (512 MB write, then read back) before every operator, outside its event pair",
                        "value_scope": "memory-bound fused kernels; GEMM timed in the same step, see ops"},
             "roofline": roofline, "ops": out_ops, "clocks": clk,
             "gpu_launches": args.steps * sum(op.launches for op in ops),

@@ -76,17 +76,6 @@ struct __align__(16) SlotEntry {
   int lo, hi_axis;        // hi_axis = hi | axis << 16
 };
 
-GBF_DEVICE void stage_slot_table(const QkvArgs& a, SlotEntry* tab) {
-  for (int p = threadIdx.x; p < a.n_slots; p += blockDim.x) {
-    SlotEntry e;
-    e.om_hi = a.omega_hi[p];
-    e.om_lo = a.omega_lo[p];
-    e.lo = a.lo_idx[p];
-    e.hi_axis = a.hi_idx[p] | (a.axis[p] << 16);
-    tab[p] = e;
-  }
-}
-
 GBF_DEVICE int64_t cache_slot(const QkvArgs& a, int64_t t, bool& ok) {
   const int64_t slot = a.slots ? static_cast<int64_t>(a.slots[t]) : t;
   ok = slot >= 0 && slot < a.cache_rows;
@@ -105,81 +94,107 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   constexpr int D = LPH * 16;
   constexpr int SLOTS = D / 2;
   constexpr int TPT = kRotGroups * LPH;     // threads per token
-  constexpr int TOK = kRotBlock / TPT;      // tokens per CTA
-  __shared__ SlotEntry tab[SLOTS];
-  stage_slot_table(a, tab);
+  constexpr int TOK = kRotBlock / TPT;      // tokens per CTA pass
+  static_assert(TOK * SLOTS == kRotBlock, "one (cos, sin) per thread and pass");
+  // (cos, sin) of the CTA's tokens: float4 [tok][i][lane] holds (cos, sin) of
+  // slots 8 lane + 2i and 8 lane + 2i + 1, so the LPH lanes of a head read
+  // consecutive float4s.  Thread (tc, p) computes slot p of token tc.
+  __shared__ float4 cs4[TOK * 4 * LPH];
+  {
+    const int tc = threadIdx.x / SLOTS, p = threadIdx.x % SLOTS;
+    const int64_t tcs = static_cast<int64_t>(blockIdx.x) * TOK + tc;
+    if (tcs < a.tokens) {
+      const float2 cs = rope_cos_sin(a.pos[tcs], a.omega_hi[p], a.omega_lo[p]);
+      float* dst = reinterpret_cast<float*>(&cs4[(tc * 4 + ((p & 7) >> 1)) * LPH + (p >> 3)]) + 2 * (p & 1);
+      dst[0] = cs.x;
+      dst[1] = cs.y;
+    }
+  }
   __syncthreads();
 
   const int lane = threadIdx.x % LPH;
   const int grp = (threadIdx.x / LPH) % kRotGroups;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * TOK + threadIdx.x / TPT;
-  if (t >= a.tokens) return;
+  const int tok = threadIdx.x / TPT;
   const int heads = a.n_q + 2 * a.n_kv;
-  const __nv_bfloat16* row = static_cast<const __nv_bfloat16*>(a.qkv) + t * static_cast<int64_t>(heads) * D;
-  bool slot_ok;
-  const int64_t crow = cache_slot(a, t, slot_ok);
-  if (!slot_ok && threadIdx.x % TPT == 0) raise_error(a.err, DEV_ERR_SLOT_RANGE);
-
-  // (cos, sin) of this lane's slots 8*lane .. 8*lane + 7
-  const int pos = a.pos[t];
-  float cs[16];
+  {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * TOK + tok;
+    if (t < a.tokens) {
+      const __nv_bfloat16* row = static_cast<const __nv_bfloat16*>(a.qkv) + t * static_cast<int64_t>(heads) * D;
+      bool slot_ok;
+      const int64_t crow = cache_slot(a, t, slot_ok);
+      if (!slot_ok && threadIdx.x % TPT == 0) raise_error(a.err, DEV_ERR_SLOT_RANGE);
+      // (cos, sin) of this lane's slots 8*lane .. 8*lane + 7, as pairs (2i, 2i + 1)
+      float2 c2[4], s2[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const SlotEntry e = tab[lane * 8 + i];
-    const float2 v = rope_cos_sin(pos, e.om_hi, e.om_lo);
-    cs[2 * i] = v.x;
-    cs[2 * i + 1] = v.y;
-  }
-
-  // Heads grp, grp + 8, ... in batches whose loads are all issued first.  The
-  // trip count depends only on grp, which all LPH lanes of a head share.
-  for (int h0 = grp; h0 < heads; h0 += kRotBatch * kRotGroups) {
-    uint4 lo[kRotBatch], hi[kRotBatch];
-#pragma unroll
-    for (int u = 0; u < kRotBatch; ++u) {
-      const int h = h0 + u * kRotGroups;
-      if (h < heads) {
-        lo[u] = ld_stream(row + h * D + lane * 8);
-        hi[u] = ld_stream(row + h * D + (lane + LPH) * 8);
+      for (int i = 0; i < 4; ++i) {
+        const float4 q = cs4[(tok * 4 + i) * LPH + lane];
+        c2[i] = make_float2(q.x, q.z);
+        s2[i] = make_float2(q.y, q.w);
       }
-    }
+
+      // Heads grp, grp + 8, ... in batches whose loads are all issued first.  The
+      // trip count depends only on grp, which all LPH lanes of a head share.
+      for (int h0 = grp; h0 < heads; h0 += kRotBatch * kRotGroups) {
+        uint4 lo[kRotBatch], hi[kRotBatch];
 #pragma unroll
-    for (int u = 0; u < kRotBatch; ++u) {
-      const int h = h0 + u * kRotGroups;
-      if (h >= heads) break;
-      if (h >= a.n_q + a.n_kv) {               // V: pass through
-        if (slot_ok) {
-          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.v_cache) +
-                               (crow * a.n_kv + (h - a.n_q - a.n_kv)) * D;
-          st_16(dst + lane * 8, lo[u]);
-          st_16(dst + (lane + LPH) * 8, hi[u]);
+        for (int u = 0; u < kRotBatch; ++u) {
+          const int h = h0 + u * kRotGroups;
+          if (h < heads) {
+            lo[u] = ld_stream(row + h * D + lane * 8);
+            hi[u] = ld_stream(row + h * D + (lane + LPH) * 8);
+          }
         }
-        continue;
-      }
-      float xl[8], xh[8];
-      bf16x8_to_f32(lo[u], xl);
-      bf16x8_to_f32(hi[u], xh);
-      float ss = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ss = fmaf(xl[i], xl[i], fmaf(xh[i], xh[i], ss));
-      ss = segment_sum(ss, LPH);               // the head's LPH lanes only
-      const bool is_q = h < a.n_q;
-      if (!is_q && !slot_ok) continue;
-      const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + a.eps);
-      const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(is_q ? a.q_w : a.k_w);
-      float wl[8], wh[8], ol[8], oh[8];
-      bf16x8_to_f32(ld_cached(w + lane * 8), wl);
-      bf16x8_to_f32(ld_cached(w + (lane + LPH) * 8), wh);
+        for (int u = 0; u < kRotBatch; ++u) {
+          const int h = h0 + u * kRotGroups;
+          if (h >= heads) break;
+          if (h >= a.n_q + a.n_kv) {               // V: pass through
+            if (slot_ok) {
+              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.v_cache) +
+                                   (crow * a.n_kv + (h - a.n_q - a.n_kv)) * D;
+              st_16(dst + lane * 8, lo[u]);
+              st_16(dst + (lane + LPH) * 8, hi[u]);
+            }
+            continue;
+          }
+          const uint32_t xl[4] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w};
+          const uint32_t xh[4] = {hi[u].x, hi[u].y, hi[u].z, hi[u].w};
+          float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float ul = xl[i] * wl[i], uh = xh[i] * wh[i];
-        ol[i] = (ul * cs[2 * i] - uh * cs[2 * i + 1]) * inv;
-        oh[i] = (uh * cs[2 * i] + ul * cs[2 * i + 1]) * inv;
+          for (int i = 0; i < 4; ++i) {
+            s0 = fma_bf16_lo(xl[i], xl[i], s0);
+            s1 = fma_bf16_hi(xl[i], xl[i], s1);
+            s0 = fma_bf16_lo(xh[i], xh[i], s0);
+            s1 = fma_bf16_hi(xh[i], xh[i], s1);
+          }
+          const float ss = segment_sum(s0 + s1, LPH);   // the head's LPH lanes only
+          const bool is_q = h < a.n_q;
+          if (!is_q && !slot_ok) continue;
+          const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + a.eps);
+          const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(is_q ? a.q_w : a.k_w);
+          const uint4 wlv = ld_cached(w + lane * 8), whv = ld_cached(w + (lane + LPH) * 8);
+          const uint32_t wl[4] = {wlv.x, wlv.y, wlv.z, wlv.w};
+          const uint32_t wh[4] = {whv.x, whv.y, whv.z, whv.w};
+          uint32_t ol[4], oh[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            // pair (8 lane + 2i + j, the same + D/2) for j = 0, 1 in the two float2 lanes
+            const float2 ul = make_float2(fma_bf16_lo(xl[i], wl[i], 0.f), fma_bf16_hi(xl[i], wl[i], 0.f));
+            const float2 uh = make_float2(fma_bf16_lo(xh[i], wh[i], 0.f), fma_bf16_hi(xh[i], wh[i], 0.f));
+            float2 rl, rh;
+            rl.x = fmaf(ul.x, c2[i].x, -(s2[i].x * uh.x)) * inv;
+            rl.y = fmaf(ul.y, c2[i].y, -(s2[i].y * uh.y)) * inv;
+            rh.x = fmaf(uh.x, c2[i].x, s2[i].x * ul.x) * inv;
+            rh.y = fmaf(uh.y, c2[i].y, s2[i].y * ul.y) * inv;
+            ol[i] = f32x2_to_bf16x2(rl.x, rl.y);
+            oh[i] = f32x2_to_bf16x2(rh.x, rh.y);
+          }
+          __nv_bfloat16* dst = is_q ? static_cast<__nv_bfloat16*>(a.q_out) + (t * a.n_q + h) * D
+                                    : static_cast<__nv_bfloat16*>(a.k_cache) + (crow * a.n_kv + (h - a.n_q)) * D;
+          st_16(dst + lane * 8, make_uint4(ol[0], ol[1], ol[2], ol[3]));
+          st_16(dst + (lane + LPH) * 8, make_uint4(oh[0], oh[1], oh[2], oh[3]));
+        }
       }
-      __nv_bfloat16* dst = is_q ? static_cast<__nv_bfloat16*>(a.q_out) + (t * a.n_q + h) * D
-                                : static_cast<__nv_bfloat16*>(a.k_cache) + (crow * a.n_kv + (h - a.n_q)) * D;
-      st_16(dst + lane * 8, f32x8_to_bf16x8(ol));
-      st_16(dst + (lane + LPH) * 8, f32x8_to_bf16x8(oh));
     }
   }
 }
@@ -564,6 +579,14 @@ cudaError_t launch_staged(const QkvArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int LPH>
+cudaError_t launch_rot1d(const QkvArgs& a, cudaStream_t stream) {
+  const int tok_per_cta = kRotBlock / (kRotGroups * LPH);
+  const unsigned grid = static_cast<unsigned>((a.tokens + tok_per_cta - 1) / tok_per_cta);
+  qkv_rot1d_kernel<LPH><<<grid, kRotBlock, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool qkv_uses_rot1d(int norm, int rope, int d) {
@@ -573,15 +596,11 @@ bool qkv_uses_rot1d(int norm, int rope, int d) {
 cudaError_t launch_qkv_split_norm_rope(const QkvArgs& a, cudaStream_t stream) {
   if (a.tokens == 0) return cudaSuccess;
   if (qkv_uses_rot1d(a.norm, a.rope, a.d)) {
-    const int lph = a.d / 16;
-    const int tok_per_cta = kRotBlock / (kRotGroups * lph);
-    const unsigned grid = static_cast<unsigned>((a.tokens + tok_per_cta - 1) / tok_per_cta);
     switch (a.d) {
-      case 64: qkv_rot1d_kernel<4><<<grid, kRotBlock, 0, stream>>>(a); break;
-      case 128: qkv_rot1d_kernel<8><<<grid, kRotBlock, 0, stream>>>(a); break;
-      default: qkv_rot1d_kernel<16><<<grid, kRotBlock, 0, stream>>>(a); break;
+      case 64: return launch_rot1d<4>(a, stream);
+      case 128: return launch_rot1d<8>(a, stream);
+      default: return launch_rot1d<16>(a, stream);
     }
-    return cudaGetLastError();
   }
   return a.norm == kQkNormFullWidth ? launch_staged<true>(a, stream) : launch_staged<false>(a, stream);
 }
