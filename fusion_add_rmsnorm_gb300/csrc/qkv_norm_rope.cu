@@ -170,7 +170,7 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
           const float ss = segment_sum(s0 + s1, LPH);   // the head's LPH lanes only
           const bool is_q = h < a.n_q;
           if (!is_q && !slot_ok) continue;
-          const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + a.eps);
+          const float inv = rsqrtf(ss / static_cast<float>(D) + a.eps);
           const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(is_q ? a.q_w : a.k_w);
           const uint4 wlv = ld_cached(w + lane * 8), whv = ld_cached(w + (lane + LPH) * 8);
           const uint32_t wl[4] = {wlv.x, wlv.y, wlv.z, wlv.w};
@@ -283,7 +283,7 @@ GBF_DEVICE void stage_vector(const QkvArgs& a, int v, uint4 xv, uint4 wv, uint32
     if (v < q_vec) ss_q += part; else ss_k += part;
   } else {
     const float hs = segment_sum(part, vph);
-    if ((threadIdx.x & (vph - 1)) == 0) inv_head[v >> lg_vph] = 1.0f / sqrtf(hs / static_cast<float>(a.d) + a.eps);
+    if ((threadIdx.x & (vph - 1)) == 0) inv_head[v >> lg_vph] = rsqrtf(hs / static_cast<float>(a.d) + a.eps);
   }
 }
 
@@ -310,7 +310,7 @@ GBF_DEVICE void rotate_vector(int v, float4 o0, float4 o1, const float pv[8], co
 }
 
 template <bool FULL>
-__global__ void __launch_bounds__(kStagedBlock, 2)
+__global__ void __launch_bounds__(kStagedBlock, 3)
 qkv_staged_kernel(const __grid_constant__ QkvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int D = a.d;
@@ -378,19 +378,31 @@ qkv_staged_kernel(const __grid_constant__ QkvArgs a) {
   auto wptr = [&](int v) -> const __nv_bfloat16* {
     return FULL ? (v < q_vec ? qw + v * 8 : kw + (v - q_vec) * 8) : (v < q_vec ? qw : kw) + P0;
   };
+  // Thread p < n_slots owns rotation slot p (the launcher guarantees
+  // blockDim.x >= n_slots).  Its grid coordinate and every thread's cache row
+  // are fetched one token ahead, off the critical path.
+  const bool cs_thread = tid < n_slots;
+  const SlotEntry my_slot = tab[cs_thread ? tid : 0];
+  auto pos_of = [&](int64_t tt) { return a.rope == kRope3D ? a.pos[tt * 3 + (my_slot.hi_axis >> 16)] : a.pos[tt]; };
+  auto row_of = [&](int64_t tt) { return a.slots ? static_cast<int64_t>(a.slots[tt]) : tt; };
+  int pos_next = cs_thread ? pos_of(blockIdx.x) : 0;
+  int64_t crow_next = row_of(blockIdx.x);
   int b = 0;                      // ring buffer of the current token
   uint32_t phase_bits = 0;        // bit j: parity of the next completion of buffer j
   for (int64_t t = blockIdx.x; t < a.tokens; t += gridDim.x) {
     const uint32_t raw32 = smem32 + static_cast<uint32_t>(b * L.raw_stride);
-    bool slot_ok;
-    const int64_t crow = cache_slot(a, t, slot_ok);
+    const int pos = pos_next;
+    const int64_t crow = crow_next;
+    if (t + gridDim.x < a.tokens) {
+      if (cs_thread) pos_next = pos_of(t + gridDim.x);
+      crow_next = row_of(t + gridDim.x);
+    }
+    const bool slot_ok = crow >= 0 && crow < a.cache_rows;
     if (!slot_ok && tid == 0) raise_error(a.err, DEV_ERR_SLOT_RANGE);
-    for (int p = tid; p < n_slots; p += blockDim.x) {
-      const SlotEntry e = tab[p];
-      const int pos = a.rope == kRope3D ? a.pos[t * 3 + (e.hi_axis >> 16)] : a.pos[t];
-      const float2 cs = rope_cos_sin(pos, e.om_hi, e.om_lo);
-      cs_pos[cs_slot(e.lo, vph)] = make_float2(cs.x, -cs.y);
-      cs_pos[cs_slot(e.hi_axis & 0xFFFF, vph)] = cs;
+    if (cs_thread) {
+      const float2 cs = rope_cos_sin(pos, my_slot.om_hi, my_slot.om_lo);
+      cs_pos[cs_slot(my_slot.lo, vph)] = make_float2(cs.x, -cs.y);
+      cs_pos[cs_slot(my_slot.hi_axis & 0xFFFF, vph)] = cs;
     }
 
     // Phase 1: x * w of Q/K to `u`, V from the ring buffer straight out.
@@ -466,8 +478,8 @@ qkv_staged_kernel(const __grid_constant__ QkvArgs a) {
       float sk = lane < nwarps ? red[2 * lane + 1] : 0.f;
       sq = warp_sum(sq);
       sk = warp_sum(sk);
-      inv_q = 1.0f / sqrtf(sq / static_cast<float>(a.n_q * D) + a.eps);
-      inv_k = 1.0f / sqrtf(sk / static_cast<float>(a.n_kv * D) + a.eps);
+      inv_q = rsqrtf(sq / static_cast<float>(a.n_q * D) + a.eps);
+      inv_k = rsqrtf(sk / static_cast<float>(a.n_kv * D) + a.eps);
     }
     if (worker) {
       float2 c2[4], s2[4];
@@ -556,22 +568,28 @@ cudaError_t launch_staged(const QkvArgs& a, cudaStream_t stream) {
   QkvArgs b = a;
   staged_shape(a, b.active, b.swz2);
   const int threads = (b.active + 31) & ~31;
+  if (threads < b.n_slots) return cudaErrorInvalidValue;   // one rotation slot per thread
   int dev = 0, sms = 0, optin = 0, per_sm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  // two ring buffers when they fit, else one (no overlap inside the CTA)
-  b.nb = 2;
-  size_t smem = staged_layout(b.n_q, b.n_kv, b.d, b.n_slots, threads / 32, b.nb).total;
-  if (smem > static_cast<size_t>(optin)) {
-    b.nb = 1;
-    smem = staged_layout(b.n_q, b.n_kv, b.d, b.n_slots, threads / 32, b.nb).total;
-    if (smem > static_cast<size_t>(optin)) return cudaErrorInvalidValue;
-  }
+  // Ring depth: the one that keeps the most CTAs on an SM (more warps hide
+  // more latency than a second buffer does), the deeper one on a tie.
   cudaError_t e = raise_smem_limit(qkv_staged_kernel<FULL>);
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qkv_staged_kernel<FULL>, threads, smem);
-  if (e != cudaSuccess) return e;
+  size_t smem = 0;
+  for (int nb = 2; nb >= 1; --nb) {
+    const size_t bytes = staged_layout(b.n_q, b.n_kv, b.d, b.n_slots, threads / 32, nb).total;
+    if (bytes > static_cast<size_t>(optin)) continue;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qkv_staged_kernel<FULL>, threads, bytes);
+    if (e != cudaSuccess) return e;
+    if (occ > per_sm) {
+      per_sm = occ;
+      b.nb = nb;
+      smem = bytes;
+    }
+  }
   if (per_sm < 1) return cudaErrorInvalidValue;
   const int64_t resident = static_cast<int64_t>(sms) * per_sm;
   const unsigned grid = static_cast<unsigned>(a.tokens < resident ? a.tokens : resident);
