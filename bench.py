@@ -44,6 +44,7 @@ import numpy as np  # noqa: E402
 METRIC = "fused-kernel HBM GB/s (% of GB300 peak) and tokens/s per fused op"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 * 10**6           # GB300 L2 capacity
 
 # ----------------------------------------------------------------- bytes model
 # Algorithmic bytes per call: every input read once, every output written once.
@@ -435,10 +436,22 @@ def kernel_traffic(op_name):
         ent = json.load(f).get("per_op", {}).get(op_name)
     if not ent:
         return None
-    src = os.path.join(ROOT, "fusion_add_rmsnorm_gb300", "csrc", ent["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != ent["source_sha256_16"]:
+    if kernel_source_hash(ent["source"]) != ent["source_sha256_16"]:
         return None
     return ent["dram_bytes_per_launch"]
+
+
+def kernel_source_hash(source):
+    """First 16 hex digits of the SHA-256 of a kernel source followed by the
+    headers every kernel includes (a change to either invalidates its record)."""
+    csrc = os.path.join(ROOT, "fusion_add_rmsnorm_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (source, "common.cuh", "tma.cuh", "kernels.h"):
+        path = os.path.join(csrc, name)
+        if not os.path.exists(path):
+            return None
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
 
 
 KERNEL_FILE = {"add_rmsnorm_fp8": "add_rmsnorm_fp8.cu", "pi05_ada_chain": "add_rmsnorm_fp8.cu",
@@ -645,9 +658,13 @@ def main_gpu(args):
     total_bytes = sum_over_ranks(pg, mem_bytes)
     value = total_bytes / (mem_ms_max / 1e3) / 1e9 if mem_ms_max > 0 else 0.0
 
-    # dominant memory-bound kernel (largest share of the step) -> roofline
-    mem_ops = [(n, d) for n, d in out_ops.items() if "gbs" in d] or [(n, dict(d, gbs=0.0))
-                                                                   for n, d in out_ops.items()]
+    # roofline: the memory-bound kernel with the largest share of the step among
+    # those whose launch moves more than L2 holds (HBM-bound by construction);
+    # the launch-bound chain of small calls is reported by its per-call latency
+    big = [(n, d) for n, d in out_ops.items()
+           if "gbs" in d and per_op[n]["op"].algorithmic_bytes() // per_op[n]["op"].launches > L2_BYTES]
+    mem_ops = big or [(n, d) for n, d in out_ops.items() if "gbs" in d] or \
+        [(n, dict(d, gbs=0.0)) for n, d in out_ops.items()]
     dom_name, dom = max(mem_ops, key=lambda kv: kv[1]["ms"])
     dom_op = per_op[dom_name]["op"]
     roofline = {"kernel": dom_name, "bound": "hbm", "achieved": dom["gbs"], "peak": peaks["hbm_gbs"],
@@ -663,6 +680,9 @@ def main_gpu(args):
                        "l2": "flushed (512 MB write, then read back) before every operator, outside its event pair",
                        "value_scope": "memory-bound fused kernels; GEMM timed in the same step, see ops"},
             "roofline": roofline, "ops": out_ops, "clocks": clk,
+            "latency_bound": {n: {"us_per_launch": round(d["ms"] * 1e3 / d["launches"], 3), "launches": d["launches"]}
+                              for n, d in out_ops.items()
+                              if "gbs" in d and per_op[n]["op"].algorithmic_bytes() // per_op[n]["op"].launches < (1 << 20)},
             "gpu_launches": args.steps * sum(op.launches for op in ops),
             "wall_s_timed_region": round(wall, 3)}
     if with_gemm and "linear_bias_gelu" in out_ops:
