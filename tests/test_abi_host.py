@@ -105,6 +105,10 @@ def test_qkv_validation(gbf):
     assert call(q=ctypes.c_void_p(5 * F + 4)) == gbf.EALIGN
     assert call(q=A(0)) == gbf.EINVAL                       # Q overlaps the packed input
     assert call(k=A(6)) == gbf.EINVAL                       # K and V caches overlap
+    # the staged (shared-memory) path bounds the row width; the per-head 1D kernel does not
+    assert call(norm=1, hq=220, hkv=40) == gbf.EUNSUPPORTED  # (6*220 + 8*40) * 128 > 196608
+    assert call(norm=0, hq=220, hkv=40, tokens=0) == gbf.OK
+    assert call(norm=1, hq=220, hkv=40, tokens=0) == gbf.EUNSUPPORTED
 
 
 def test_linear_and_fold_and_copy_validation(gbf):
