@@ -23,8 +23,11 @@
 //   warps 4-7  epilogue: tcgen05.ld 32 columns at a time (warp w reads TMEM
 //              lanes 32 (w % 4) .. +31, one output row per thread), add bias,
 //              GELU, round to bf16, 16-byte stores.
-// Tiles are visited m-fastest, so the CTAs working at one time share one
-// column block of W and all of X, which stay in L2.
+// Tile order: the N tiles are cut into groups of kGroupN; inside a group the
+// tiles run n-fastest, so the CTAs working at one time cover about ten 128-row
+// blocks of X against the group's kGroupN W column blocks.  A group's W
+// (kGroupN x 2 MB at K = 4096) stays in L2 while X streams past it once per
+// group, instead of all of X having to stay in L2 for every W column block.
 //
 // Every mbarrier wait is bounded (about one second of wall time): a wait that
 // gives up sets DEV_ERR_MBAR_TIMEOUT in the device error word and raises a
@@ -127,6 +130,8 @@ GBF_DEVICE float gelu_tanh(float a) {
   return 0.5f * a * (1.0f + tanhf(inner));
 }
 
+constexpr int kGroupN = 16;
+
 struct GemmParams {
   const __nv_bfloat16* bias;
   __nv_bfloat16* y;
@@ -135,6 +140,17 @@ struct GemmParams {
   int m_tiles, n_tiles;
   int act;
 };
+
+// Output tile origin (m0, n0) of linear tile index `tile` (see the tile order above).
+GBF_DEVICE void tile_origin(const GemmParams& p, int tile, int& m0, int& n0) {
+  const int per_group = kGroupN * p.m_tiles;
+  const int g = tile / per_group;
+  const int idx = tile - g * per_group;
+  const int n_base = g * kGroupN;
+  const int gs = p.n_tiles - n_base < kGroupN ? p.n_tiles - n_base : kGroupN;
+  m0 = (idx / gs) * BM;
+  n0 = (n_base + idx % gs) * BN;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
@@ -184,8 +200,8 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       uint32_t issued[STAGES] = {};        // phases issued per stage (for the final drain)
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile % p.m_tiles) * BM;
-        const int n0 = (tile / p.m_tiles) * BN;
+        int m0, n0;
+        tile_origin(p, tile, m0, n0);
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, &ctl->abort, p.err)) {
             ok = false;
@@ -260,8 +276,8 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      const int m0 = (tile % p.m_tiles) * BM;
-      const int n0 = (tile / p.m_tiles) * BN;
+      int m0, n0;
+      tile_origin(p, tile, m0, n0);
       const int row = m0 + quarter * 32 + lane;
       __nv_bfloat16* yrow = p.y + static_cast<int64_t>(row) * p.n;
       const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
