@@ -84,12 +84,27 @@ def test_all_combinations(gbf, norm, rope, tokens, hq, hkv, d):
 @pytest.mark.parametrize("norm", [0, 1])
 @pytest.mark.parametrize("rope", [0, 1])
 def test_many_heads_two_pass_path(gbf, norm, rope):
-    """80 Q/K heads of width 256: more heads per thread than the single-pass
-    kernel keeps in registers, so the two-pass kernel runs."""
+    """80 Q/K heads of width 256 (48 KB rows): several heads per thread in every
+    kernel, and the smallest ring the streamed kernels pick for such rows."""
     sections = (86, 86, 84) if rope else None
     c = workloads.qkv_case(7, 64, 16, 256, norm, rope, seed=31 + norm + 2 * rope, theta=1e4,
                            grid=(2, 2, 2) if rope else None, sections=sections)
     check(gbf, c, f"two-pass norm {norm} rope {rope}")
+
+
+def test_per_head_1d_wide_rows(gbf):
+    """Per-head 1D rows of 160 heads x 256 (80 KB): 20 heads per lane group and
+    a batch of loads cut short at the end; an odd token count leaves a partial
+    last CTA."""
+    c = workloads.qkv_case(9, 96, 32, 256, 0, 0, seed=53, theta=1e6)
+    check(gbf, c, "per-head 1D, wide rows")
+
+
+@pytest.mark.parametrize("tokens", [1, 2, 3, 1000])
+def test_per_head_1d_token_counts(gbf, tokens):
+    """Token counts that fill one, part of one, and many CTAs of four tokens."""
+    c = workloads.qkv_case(tokens, 8, 2, 128, 0, 0, seed=60 + tokens, theta=1e6)
+    check(gbf, c, f"per-head 1D, {tokens} tokens")
 
 
 @pytest.mark.parametrize("rope", [0, 1])
