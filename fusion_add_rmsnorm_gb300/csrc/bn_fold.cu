@@ -32,6 +32,8 @@ GBF_DEVICE float fold_scale(const BnFoldArgs& a, int64_t c) {
 
 template <bool VEC>
 __global__ void __launch_bounds__(kBnBlock) bn_fold_kernel(const BnFoldArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kBnBlock + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kBnBlock) >> 5;
@@ -84,11 +86,8 @@ cudaError_t launch_bn_fold(const BnFoldArgs& a, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
   const bool vec = (a.inner % 8 == 0) && (reinterpret_cast<uintptr_t>(a.w) % 16 == 0) &&
                    (reinterpret_cast<uintptr_t>(a.w_out) % 16 == 0);
-  if (vec)
-    bn_fold_kernel<true><<<grid, kBnBlock, 0, stream>>>(a);
-  else
-    bn_fold_kernel<false><<<grid, kBnBlock, 0, stream>>>(a);
-  return cudaGetLastError();
+  return vec ? launch_pdl(bn_fold_kernel<true>, dim3(grid), dim3(kBnBlock), 0, stream, a)
+             : launch_pdl(bn_fold_kernel<false>, dim3(grid), dim3(kBnBlock), 0, stream, a);
 }
 
 }  // namespace gbf

@@ -144,4 +144,24 @@ GBF_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); 
 // Allow the next grid in the stream to begin launching.
 GBF_DEVICE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
+// Launch `kernel` with programmatic stream serialisation: its CTAs may be
+// scheduled while the previous kernel in the stream is finishing, and they
+// wait for that kernel (completion and memory) in pdl_wait(), which every
+// kernel launched this way calls before its first global memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace gbf

@@ -96,6 +96,8 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   constexpr int TPT = kRotGroups * LPH;     // threads per token
   constexpr int TOK = kRotBlock / TPT;      // tokens per CTA pass
   static_assert(TOK * SLOTS == kRotBlock, "one (cos, sin) per thread and pass");
+  pdl_wait();
+  pdl_launch_dependents();
   // (cos, sin) of the CTA's tokens: float4 [tok][i][lane] holds (cos, sin) of
   // slots 8 lane + 2i and 8 lane + 2i + 1, so the LPH lanes of a head read
   // consecutive float4s.  Thread (tc, p) computes slot p of token tc.
@@ -313,6 +315,8 @@ template <bool FULL>
 __global__ void __launch_bounds__(kStagedBlock, 3)
 qkv_staged_kernel(const __grid_constant__ QkvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_wait();
+  pdl_launch_dependents();
   const int D = a.d;
   const int vph = D >> 3;
   const int n_slots = a.n_slots;
@@ -593,16 +597,14 @@ cudaError_t launch_staged(const QkvArgs& a, cudaStream_t stream) {
   if (per_sm < 1) return cudaErrorInvalidValue;
   const int64_t resident = static_cast<int64_t>(sms) * per_sm;
   const unsigned grid = static_cast<unsigned>(a.tokens < resident ? a.tokens : resident);
-  qkv_staged_kernel<FULL><<<grid, threads, smem, stream>>>(b);
-  return cudaGetLastError();
+  return launch_pdl(qkv_staged_kernel<FULL>, dim3(grid), dim3(threads), smem, stream, b);
 }
 
 template <int LPH>
 cudaError_t launch_rot1d(const QkvArgs& a, cudaStream_t stream) {
   const int tok_per_cta = kRotBlock / (kRotGroups * LPH);
   const unsigned grid = static_cast<unsigned>((a.tokens + tok_per_cta - 1) / tok_per_cta);
-  qkv_rot1d_kernel<LPH><<<grid, kRotBlock, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(qkv_rot1d_kernel<LPH>, dim3(grid), dim3(kRotBlock), 0, stream, a);
 }
 
 }  // namespace
