@@ -84,7 +84,7 @@ GBF_DEVICE int64_t cache_slot(const QkvArgs& a, int64_t t, bool& ok) {
 
 // --------------------------------------------------------- per-head, 1D
 
-constexpr int kRotGroups = 8;               // head groups per token
+constexpr int kRotGroups = 16;              // head groups per token
 constexpr int kRotBlock = 256;
 constexpr int kRotBatch = 3;                // heads whose loads are in flight together
 
@@ -95,7 +95,7 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   constexpr int SLOTS = D / 2;
   constexpr int TPT = kRotGroups * LPH;     // threads per token
   constexpr int TOK = kRotBlock / TPT;      // tokens per CTA pass
-  static_assert(TOK * SLOTS == kRotBlock, "one (cos, sin) per thread and pass");
+  static_assert(TOK * SLOTS <= kRotBlock, "at most one (cos, sin) per thread");
   pdl_wait();
   pdl_launch_dependents();
   // (cos, sin) of the CTA's tokens: float4 [tok][i][lane] holds (cos, sin) of
@@ -105,7 +105,7 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   {
     const int tc = threadIdx.x / SLOTS, p = threadIdx.x % SLOTS;
     const int64_t tcs = static_cast<int64_t>(blockIdx.x) * TOK + tc;
-    if (tcs < a.tokens) {
+    if (tc < TOK && tcs < a.tokens) {
       const float2 cs = rope_cos_sin(a.pos[tcs], a.omega_hi[p], a.omega_lo[p]);
       float* dst = reinterpret_cast<float*>(&cs4[(tc * 4 + ((p & 7) >> 1)) * LPH + (p >> 3)]) + 2 * (p & 1);
       dst[0] = cs.x;
