@@ -98,6 +98,28 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   static_assert(TOK * SLOTS <= kRotBlock, "at most one (cos, sin) per thread");
   pdl_wait();
   pdl_launch_dependents();
+  const int lane = threadIdx.x % LPH;
+  const int grp = (threadIdx.x / LPH) % kRotGroups;
+  const int tok = threadIdx.x / TPT;
+  const int heads = a.n_q + 2 * a.n_kv;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * TOK + tok;
+  const bool live = t < a.tokens;
+  const __nv_bfloat16* row = static_cast<const __nv_bfloat16*>(a.qkv) + t * static_cast<int64_t>(heads) * D;
+  // Heads grp, grp + kRotGroups, ... in batches whose loads are all issued
+  // first; the first batch is requested before the (cos, sin) table is built.
+  uint4 lo[kRotBatch], hi[kRotBatch];
+  auto load_batch = [&](int h0) {
+#pragma unroll
+    for (int u = 0; u < kRotBatch; ++u) {
+      const int h = h0 + u * kRotGroups;
+      if (h < heads) {
+        lo[u] = ld_stream(row + h * D + lane * 8);
+        hi[u] = ld_stream(row + h * D + (lane + LPH) * 8);
+      }
+    }
+  };
+  if (live) load_batch(grp);
+
   // (cos, sin) of the CTA's tokens: float4 [tok][i][lane] holds (cos, sin) of
   // slots 8 lane + 2i and 8 lane + 2i + 1, so the LPH lanes of a head read
   // consecutive float4s.  Thread (tc, p) computes slot p of token tc.
@@ -114,14 +136,8 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   }
   __syncthreads();
 
-  const int lane = threadIdx.x % LPH;
-  const int grp = (threadIdx.x / LPH) % kRotGroups;
-  const int tok = threadIdx.x / TPT;
-  const int heads = a.n_q + 2 * a.n_kv;
   {
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * TOK + tok;
-    if (t < a.tokens) {
-      const __nv_bfloat16* row = static_cast<const __nv_bfloat16*>(a.qkv) + t * static_cast<int64_t>(heads) * D;
+    if (live) {
       bool slot_ok;
       const int64_t crow = cache_slot(a, t, slot_ok);
       if (!slot_ok && threadIdx.x % TPT == 0) raise_error(a.err, DEV_ERR_SLOT_RANGE);
@@ -134,18 +150,9 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
         s2[i] = make_float2(q.y, q.w);
       }
 
-      // Heads grp, grp + 8, ... in batches whose loads are all issued first.  The
-      // trip count depends only on grp, which all LPH lanes of a head share.
+      // The trip count depends only on grp, which all LPH lanes of a head share.
       for (int h0 = grp; h0 < heads; h0 += kRotBatch * kRotGroups) {
-        uint4 lo[kRotBatch], hi[kRotBatch];
-#pragma unroll
-        for (int u = 0; u < kRotBatch; ++u) {
-          const int h = h0 + u * kRotGroups;
-          if (h < heads) {
-            lo[u] = ld_stream(row + h * D + lane * 8);
-            hi[u] = ld_stream(row + h * D + (lane + LPH) * 8);
-          }
-        }
+        if (h0 != grp) load_batch(h0);
 #pragma unroll
         for (int u = 0; u < kRotBatch; ++u) {
           const int h = h0 + u * kRotGroups;
