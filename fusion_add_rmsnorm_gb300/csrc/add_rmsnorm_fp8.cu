@@ -21,6 +21,9 @@
 // that bf16 value; y = r_hat * inv * w (or * (1 + scale) + shift) stays in
 // float32 registers with the descale 1/s folded into the per-column factors;
 // code = e4m3_rne_sat(y / s).
+#include <map>
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -198,26 +201,6 @@ add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
   }
 }
 
-template <int MODE, bool GATED>
-cudaError_t launch_mode(const AddRmsNormArgs& a, int nv, dim3 grid, dim3 block, cudaStream_t s, bool pdl) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  switch (nv) {
-    case 1: return cudaLaunchKernelEx(&cfg, add_rmsnorm_fp8_kernel<MODE, GATED, 1>, a);
-    case 2: return cudaLaunchKernelEx(&cfg, add_rmsnorm_fp8_kernel<MODE, GATED, 2>, a);
-    case 4: return cudaLaunchKernelEx(&cfg, add_rmsnorm_fp8_kernel<MODE, GATED, 4>, a);
-    case 8: return cudaLaunchKernelEx(&cfg, add_rmsnorm_fp8_kernel<MODE, GATED, 8>, a);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -228,6 +211,50 @@ int sm_count() {
   }
   return n;
 }
+
+// CTAs of `kern` with `block` threads that fit on one SM (cached per kernel
+// and block size; the persistent grid is capped at that many per SM).
+template <typename K>
+int resident_per_sm(K kern, int block) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kern), block);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, block, 0) != cudaSuccess || occ < 1) occ = 1;
+  cache[key] = occ;
+  return occ;
+}
+
+template <int MODE, bool GATED, int NV>
+cudaError_t launch_nv(const AddRmsNormArgs& a, int64_t blocks, dim3 block, cudaStream_t s, bool pdl) {
+  auto kern = add_rmsnorm_fp8_kernel<MODE, GATED, NV>;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * resident_per_sm(kern, static_cast<int>(block.x));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks < cap ? blocks : cap));
+  cfg.blockDim = block;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int MODE, bool GATED>
+cudaError_t launch_mode(const AddRmsNormArgs& a, int nv, int64_t blocks, dim3 block, cudaStream_t s, bool pdl) {
+  switch (nv) {
+    case 1: return launch_nv<MODE, GATED, 1>(a, blocks, block, s, pdl);
+    case 2: return launch_nv<MODE, GATED, 2>(a, blocks, block, s, pdl);
+    case 4: return launch_nv<MODE, GATED, 4>(a, blocks, block, s, pdl);
+    case 8: return launch_nv<MODE, GATED, 8>(a, blocks, block, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 
 }  // namespace
 
@@ -245,10 +272,8 @@ AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden) {
   // Small rows share a CTA of 256 threads; large rows get a CTA each.
   p.rows_per_cta = tpr >= 256 ? 1 : 256 / tpr;
   p.block = tpr * p.rows_per_cta;
-  const int64_t blocks = rows == 0 ? 0 : (rows + p.rows_per_cta - 1) / p.rows_per_cta;
-  // Persistent: at most 2048 / block CTAs per SM.
-  const int64_t cap = static_cast<int64_t>(sm_count()) * (2048 / p.block);
-  p.grid = blocks < cap ? blocks : cap;
+  // CTAs needed; the launch caps the persistent grid at the CTAs that fit at once
+  p.grid = rows == 0 ? 0 : (rows + p.rows_per_cta - 1) / p.rows_per_cta;
   return p;
 }
 
@@ -258,18 +283,19 @@ cudaError_t launch_add_rmsnorm_fp8(AddRmsNormArgs a, cudaStream_t stream, bool p
   if (p.grid == 0) return cudaSuccess;
   a.tpr = p.tpr;
   a.rows_per_cta = p.rows_per_cta;
-  const dim3 grid(static_cast<unsigned>(p.grid)), block(static_cast<unsigned>(p.block));
+  const int64_t blocks = p.grid;
+  const dim3 block(static_cast<unsigned>(p.block));
   const bool gated = a.gate != nullptr;
   switch (a.mode) {
     case kNormWeight:
-      return gated ? launch_mode<kNormWeight, true>(a, p.nv, grid, block, stream, pdl)
-                   : launch_mode<kNormWeight, false>(a, p.nv, grid, block, stream, pdl);
+      return gated ? launch_mode<kNormWeight, true>(a, p.nv, blocks, block, stream, pdl)
+                   : launch_mode<kNormWeight, false>(a, p.nv, blocks, block, stream, pdl);
     case kNormNoWeight:
-      return gated ? launch_mode<kNormNoWeight, true>(a, p.nv, grid, block, stream, pdl)
-                   : launch_mode<kNormNoWeight, false>(a, p.nv, grid, block, stream, pdl);
+      return gated ? launch_mode<kNormNoWeight, true>(a, p.nv, blocks, block, stream, pdl)
+                   : launch_mode<kNormNoWeight, false>(a, p.nv, blocks, block, stream, pdl);
     case kNormAda:
-      return gated ? launch_mode<kNormAda, true>(a, p.nv, grid, block, stream, pdl)
-                   : launch_mode<kNormAda, false>(a, p.nv, grid, block, stream, pdl);
+      return gated ? launch_mode<kNormAda, true>(a, p.nv, blocks, block, stream, pdl)
+                   : launch_mode<kNormAda, false>(a, p.nv, blocks, block, stream, pdl);
     default:
       return cudaErrorInvalidValue;
   }

@@ -34,7 +34,7 @@ struct AddRmsNormArgs {
 struct AddRmsNormPlan {
   bool ok;
   int nv, tpr, rows_per_cta, block;
-  int64_t grid;
+  int64_t grid;           // CTAs needed; the launch caps it at the CTAs that fit on the GPU at once
 };
 
 AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden);
