@@ -806,6 +806,54 @@ def main_reference(args):
     print(json.dumps(line))
 
 
+def main_sweep(args):
+    """`--sweep`: the add+RMSNorm+FP8 kernel over rows x hidden x mode, one JSON
+    line per point (HBM GB/s and fraction of the measured copy bandwidth).
+    Inputs come from torch's seeded generator on the device, drawn as the
+    workloads draw them (x, res ~ N(0,1); weight 1+N(0,0.1); gate, shift,
+    scale ~ N(0,0.2)); throughput does not depend on the values."""
+    import torch
+    import fusion_add_rmsnorm_gb300 as gbf
+    peaks = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_words = flush.view(torch.int64)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    for rows in (4096, 16384, 65536):
+        for hidden in (1024, 4096, 8192):
+            bf = dict(dtype=torch.bfloat16, device="cuda")
+            x = torch.randn(rows, hidden, generator=gen, **bf)
+            res = torch.randn(rows, hidden, generator=gen, **bf)
+            out = torch.empty_like(res)
+            q = torch.empty(rows, hidden, dtype=torch.uint8, device="cuda")
+            vec = lambda m, sd: (m + sd * torch.randn(hidden, generator=gen, device="cuda")).to(torch.bfloat16)  # noqa
+            w, gate, scale, shift = vec(1.0, 0.1), vec(0.0, 0.2), vec(0.0, 0.2), vec(0.0, 0.2)
+            for name, mode, gated in (("weighted", 0, False), ("noweight", 1, False), ("ada", 2, True)):
+                def call():
+                    gbf.add_rmsnorm_fp8(x, res, out, q, mode, weight=w if mode == 0 else None,
+                                        gate=gate if gated else None, ada_scale=scale if mode == 2 else None,
+                                        ada_shift=shift if mode == 2 else None, eps=1e-6, fp8_scale=0.05)
+                ts = []
+                for it in range(args.warmup + args.steps):
+                    flush.fill_(1)
+                    flush_words.sum()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    call()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    if it >= args.warmup:
+                        ts.append(e0.elapsed_time(e1))
+                ms = sorted(ts)[len(ts) // 2]
+                nbytes = bytes_add_rmsnorm(rows, hidden, mode, gated)
+                gbs = nbytes / (ms / 1e3) / 1e9
+                print(json.dumps({"sweep": "add_rmsnorm_fp8", "mode": name, "rows": rows, "hidden": hidden,
+                                  "us_median": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+                                  "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                                  "l2_flushed": True, "timed_calls": args.steps}), flush=True)
+            del x, res, out, q
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -817,8 +865,13 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     ap.add_argument("--only", default="", help="comma-separated subset of: " + ", ".join(OP_NAMES))
     ap.add_argument("--small", action="store_true", help="profiling-size cases (still larger than L2)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="add+RMSNorm+FP8 over rows {4096, 16384, 65536} x hidden {1024, 4096, 8192} x 3 modes")
     ap.add_argument("--_cpu-baseline-child", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.sweep:
+        main_sweep(args)
+        return
     if args._cpu_baseline_child:
         print(json.dumps(cpu_baseline_sample(args._cpu_baseline_child)))
         return

@@ -261,9 +261,15 @@ cudaError_t launch_mode(const AddRmsNormArgs& a, int nv, int64_t blocks, dim3 bl
 AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden) {
   AddRmsNormPlan p = {};
   const int64_t nvec = hidden / 8;
-  // Up to 512 threads per row, then more vectors per thread.
+  // Vectors per thread: 1 for launch-bound shapes (the most threads per row,
+  // the shortest critical path); 2 once there are at least four vectors per
+  // thread the GPU holds at once (half the per-row reduction and loop work per
+  // element); more when a row would need more than kMaxBlock threads.  Rows
+  // keep at least 8 threads.
+  const bool large = rows * nvec >= 4LL * sm_count() * 2048;
+  const int target = large ? 2 : 1;
   int nv = 1;
-  while (nv < 8 && nvec > static_cast<int64_t>(nv) * kMaxBlock) nv *= 2;
+  while (nv < 8 && ((nv < target && nvec >= 16 * nv) || nvec > static_cast<int64_t>(nv) * kMaxBlock)) nv *= 2;
   int tpr = 8;
   while (static_cast<int64_t>(tpr) * nv < nvec) tpr *= 2;
   p.ok = static_cast<int64_t>(tpr) * nv >= nvec && tpr <= kMaxBlock;
