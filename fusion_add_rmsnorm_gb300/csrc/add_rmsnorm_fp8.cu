@@ -31,6 +31,9 @@ namespace gbf {
 namespace {
 
 constexpr int kMaxBlock = 512;
+// Threads per CTA of the NV-vector kernel: rows of two vectors per thread use
+// at most 256 threads, so three CTAs fit on an SM.
+constexpr int max_block(int nv) { return nv == 2 ? 256 : kMaxBlock; }
 
 GBF_DEVICE uint4 bf16x8_add(uint4 a, uint4 b) {
   uint4 r;
@@ -55,7 +58,7 @@ GBF_DEVICE uint4 bf16x8_fma(uint4 g, uint4 x, uint4 r0) {
 }
 
 template <int MODE, bool GATED, int NV>
-__global__ void __launch_bounds__(kMaxBlock)
+__global__ void __launch_bounds__(max_block(NV), NV == 2 ? 3 : 1)
 add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
   // Rows of up to 2 vectors per thread keep the per-column factors and the
   // next row's inputs in registers; wider rows (BIG) reload the factors from
@@ -269,10 +272,10 @@ AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden) {
   const bool large = rows * nvec >= 4LL * sm_count() * 2048;
   const int target = large ? 2 : 1;
   int nv = 1;
-  while (nv < 8 && ((nv < target && nvec >= 16 * nv) || nvec > static_cast<int64_t>(nv) * kMaxBlock)) nv *= 2;
+  while (nv < 8 && ((nv < target && nvec >= 16 * nv) || nvec > static_cast<int64_t>(nv) * max_block(nv))) nv *= 2;
   int tpr = 8;
   while (static_cast<int64_t>(tpr) * nv < nvec) tpr *= 2;
-  p.ok = static_cast<int64_t>(tpr) * nv >= nvec && tpr <= kMaxBlock;
+  p.ok = static_cast<int64_t>(tpr) * nv >= nvec && tpr <= max_block(nv);
   p.nv = nv;
   p.tpr = tpr;
   // Small rows share a CTA of 256 threads; large rows get a CTA each.
