@@ -60,10 +60,14 @@ GBF_DEVICE uint4 bf16x8_fma(uint4 g, uint4 x, uint4 r0) {
 template <int MODE, bool GATED, int NV>
 __global__ void __launch_bounds__(max_block(NV), NV == 2 ? 3 : 1)
 add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
-  // Rows of up to 2 vectors per thread keep the per-column factors and the
-  // next row's inputs in registers; wider rows (BIG) reload the factors from
-  // L1 and issue their loads at the top of each row to stay within registers.
+  // Rows of up to 2 vectors per thread keep the next row's inputs in
+  // registers (prefetch); wider rows (BIG) issue their loads at the top of
+  // each row.  The per-column factors stay in registers (REGF) for 1 vector
+  // per thread, and for 2 unless the mode is AdaRMSNorm (two factor vectors
+  // plus the gate); otherwise they are reloaded from L1 every row, which keeps
+  // three CTAs per SM.
   constexpr bool BIG = NV > 2;
+  constexpr bool REGF = NV == 1 || (NV == 2 && MODE != kNormAda);
   const int tpr = a.tpr;
   const int lane = threadIdx.x & (tpr - 1);
   const int row_in_cta = threadIdx.x / tpr;
@@ -101,10 +105,10 @@ add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
       }
     }
   };
-  constexpr int NF = BIG ? 1 : NV;
+  constexpr int NF = REGF ? NV : 1;
   float fa[NF][8], fb[NF][8];
   uint4 gate[NF];
-  if (!BIG) {
+  if (REGF) {
 #pragma unroll
     for (int k = 0; k < NF; ++k) {
       if (!vok[k]) continue;
@@ -155,8 +159,8 @@ add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
       for (int k = 0; k < NV; ++k) {
         if (!vok[k]) continue;
         if (GATED) {
-          const uint4 g = BIG ? ld_cached(static_cast<const __nv_bfloat16*>(a.gate) + (lane + k * tpr) * 8)
-                              : gate[BIG ? 0 : k];
+          const uint4 g = REGF ? gate[REGF ? k : 0]
+                               : ld_cached(static_cast<const __nv_bfloat16*>(a.gate) + (lane + k * tpr) * 8);
           rh[k] = bf16x8_fma(g, cx[k], cr[k]);
         } else {
           rh[k] = bf16x8_add(cx[k], cr[k]);
@@ -185,9 +189,9 @@ add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
       float h[8], q[8];
       bf16x8_to_f32(rh[k], h);
       float fbig_a[8], fbig_b[8];
-      const float* fak = BIG ? fbig_a : fa[BIG ? 0 : k];
-      const float* fbk = BIG ? fbig_b : fb[BIG ? 0 : k];
-      if (BIG) factors(k, fbig_a, fbig_b);
+      const float* fak = REGF ? fa[REGF ? k : 0] : fbig_a;
+      const float* fbk = REGF ? fb[REGF ? k : 0] : fbig_b;
+      if (!REGF) factors(k, fbig_a, fbig_b);
       if (MODE == kNormWeight) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) q[i] = (h[i] * inv) * fak[i];
