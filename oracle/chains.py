@@ -15,7 +15,7 @@ from . import ops
 from .formats import bf16_decode, bf16_encode, bf16_round
 
 NORM_WEIGHT, NORM_NOWEIGHT, NORM_ADA = 0, 1, 2
-QKNORM_PER_HEAD, QKNORM_FULL_WIDTH = 0, 1
+QKNORM_PER_HEAD, QKNORM_FULL_WIDTH, QKNORM_LAYERNORM = 0, 1, 2
 ROPE_1D, ROPE_3D = 0, 1
 
 
@@ -63,14 +63,17 @@ def add_rmsnorm_fp8(x, res, eps, s_q, mode, weight=None, gate=None,
 
 def qkv_split_norm_rope(qkv, n_q_heads, n_kv_heads, head_dim, norm, q_w, k_w, eps,
                         rope, pos, theta, sections=None, slots=None, cache_rows=None,
-                        rope3d=None):
+                        rope3d=None, q_b=None, k_b=None):
     """Packed-QKV post-processing: split -> Q/K RMSNorm -> RoPE -> write Q and
     the K/V cache; V passes through (FlashRT §2.2: Qwen3 q_norm/k_norm + RoPE +
     KV-cache write; Wan packed-QKV split + two RMSNorms + 3D RoPE; the shared
     contract "Q/K norm -> RoPE, V direct").
 
     qkv: bf16 bits [T, (Hq + 2 Hkv) * D]; q_w, k_w: bf16 bits [D] (per head) or
-    [H * D] (full width); pos: int32 [T] (1D) or [T, 3] (3D).  The K and V rows
+    [H * D] (full width); pos: int32 [T] (1D) or [T, 3] (3D).  norm
+    QKNORM_LAYERNORM is a per-head LayerNorm instead of the RMSNorm
+    (FlashRT §2.2, Chameleon prefill: LayerNorm(Q) + LayerNorm(K) + rotate_half
+    RoPE), with optional bf16 biases q_b, k_b [D] (None: 0).  The K and V rows
     of token t go to cache row slots[t] (row t when slots is None) of caches
     holding cache_rows rows (T when None).  Returns bf16 bits
     (q [T, Hq, D], k_cache [cache_rows, Hkv, D], v_cache [cache_rows, Hkv, D]);
@@ -91,6 +94,9 @@ def qkv_split_norm_rope(qkv, n_q_heads, n_kv_heads, head_dim, norm, q_w, k_w, ep
     elif norm == QKNORM_FULL_WIDTH:
         qn = ops.qk_rmsnorm_full_width(q, qw, eps)
         kn = ops.qk_rmsnorm_full_width(k, kw, eps)
+    elif norm == QKNORM_LAYERNORM:
+        qn = ops.qk_layernorm_per_head(q, qw, None if q_b is None else bf16_decode(q_b), eps)
+        kn = ops.qk_layernorm_per_head(k, kw, None if k_b is None else bf16_decode(k_b), eps)
     else:
         raise ValueError(f"unknown qk-norm mode {norm}")
     if rope == ROPE_1D:

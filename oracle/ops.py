@@ -177,6 +177,30 @@ def qk_rmsnorm_full_width(u, weight, eps):
     return rmsnorm(flat, eps, np.asarray(weight, np.float64)[None, :], axis=-1).reshape(t, h, d)
 
 
+def layernorm(u, eps, weight=None, bias=None, axis=-1):
+    """LayerNorm over `axis`: mu = mean(u), var = mean((u - mu)**2),
+    y = (u - mu) / sqrt(var + eps) * w + b (a missing weight is 1, a missing
+    bias 0).  Two passes over the values: the mean first, then the centred
+    squares."""
+    u = np.asarray(u, np.float64)
+    mu = np.mean(u, axis=axis, keepdims=True)
+    c = u - mu
+    var = np.mean(c * c, axis=axis, keepdims=True)
+    y = c / np.sqrt(var + eps)
+    if weight is not None:
+        y = y * np.asarray(weight, np.float64)
+    if bias is not None:
+        y = y + np.asarray(bias, np.float64)
+    return y
+
+
+def qk_layernorm_per_head(u, weight, bias, eps):
+    """LayerNorm of every head over its head_dim, weight and bias indexed by d
+    (the LayerNorm(Q) + LayerNorm(K) of FlashRT §2.2, Chameleon prefill path)."""
+    return layernorm(u, eps, np.asarray(weight, np.float64)[None, None, :],
+                     None if bias is None else np.asarray(bias, np.float64)[None, None, :], axis=-1)
+
+
 # ------------------------------------------------------- Linear and GELU
 
 

@@ -128,6 +128,26 @@ def test_qkv_rotation_reaches_q_and_k_but_not_v():
     assert np.array_equal(zero[2], rot[2])
 
 
+def test_qkv_layernorm_constant_heads_give_their_own_bias():
+    """LayerNorm mode: a head whose values are all equal normalises to its
+    bias exactly, and position 0 does not rotate, so Q carries q_b and K
+    carries k_b bit for bit (each head its own constant); V is copied."""
+    rng = np.random.default_rng(31)
+    t, hq, hkv, d = 3, 2, 2, 16
+    consts = rng.normal(size=(t, hq + 2 * hkv, 1))
+    qkv = bf16_encode(np.broadcast_to(consts, (t, hq + 2 * hkv, d)).reshape(t, -1))
+    qw, kw = _rand_bits(rng, d, 1, .1), _rand_bits(rng, d, 1, .1)
+    qb, kb = _rand_bits(rng, d, 0, .5), _rand_bits(rng, d, 0, .5)
+    q, kc, vc = chains.qkv_split_norm_rope(qkv, hq, hkv, d, chains.QKNORM_LAYERNORM, qw, kw, 1e-5, 0,
+                                           np.zeros(t, np.int32), 1e4, q_b=qb, k_b=kb)
+    assert np.array_equal(q, np.broadcast_to(qb, q.shape))
+    assert np.array_equal(kc, np.broadcast_to(kb, kc.shape))
+    assert np.array_equal(vc, qkv.reshape(t, hq + 2 * hkv, d)[:, hq + hkv:])
+    q0, k0, _ = chains.qkv_split_norm_rope(qkv, hq, hkv, d, chains.QKNORM_LAYERNORM, qw, kw, 1e-5, 0,
+                                           np.zeros(t, np.int32), 1e4)
+    assert not q0.any() and not k0.any()             # no bias: exactly zero
+
+
 def test_qkv_slots_permute_cache_rows():
     rng = np.random.default_rng(24)
     t, hq, hkv, d = 6, 2, 1, 8

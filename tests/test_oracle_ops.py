@@ -81,6 +81,57 @@ def test_full_width_norm_uses_one_scale_per_token():
 
 # --------------------------------------------------------------------- RoPE
 
+@pytest.mark.parametrize("c", [3.0, -0.25, 1e-3])
+def test_layernorm_of_constant_vector_is_the_bias(c):
+    """A constant vector has no deviation from its mean: the output is b
+    exactly, whatever the weight and eps."""
+    w = np.array([0.5, -2.0, 3.0, 1.5, 0.75])
+    b = np.array([0.1, -0.2, 0.3, 0.0, 5.0])
+    assert np.array_equal(ops.layernorm(np.full((2, 5), c), 1e-5, w, b), np.tile(b, (2, 1)))
+
+
+def test_layernorm_worked_example():
+    """x = (1, 2, 3, 4), eps = 0: mean 2.5, variance 1.25, so
+    y = (x - 2.5) / sqrt(1.25) = (-3, -1, 1, 3) / sqrt(5)."""
+    y = ops.layernorm(np.array([1.0, 2.0, 3.0, 4.0]), 0.0)
+    assert np.allclose(y, np.array([-3.0, -1.0, 1.0, 3.0]) / np.sqrt(5.0), rtol=0, atol=1e-15)
+
+
+def test_layernorm_shift_and_scale_invariance_and_moments():
+    """LN(a x + c) = LN(x) for a > 0 at eps = 0; with w = 1, b = 0 the output
+    has mean 0 and variance var / (var + eps)."""
+    x = np.random.default_rng(5).normal(size=(7, 64)) * 3 + 1
+    base = ops.layernorm(x, 0.0)
+    assert np.allclose(ops.layernorm(2.5 * x - 7.0, 0.0), base, rtol=0, atol=1e-12)
+    eps = 0.3
+    y = ops.layernorm(x, eps)
+    var = x.var(axis=-1)
+    assert np.allclose(y.mean(axis=-1), 0, atol=1e-13)
+    assert np.allclose(y.var(axis=-1), var / (var + eps), rtol=1e-12)
+
+
+def test_layernorm_matches_torch_layer_norm_fp64():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(6)
+    x, w, b = rng.normal(size=(5, 128)), rng.normal(size=128), rng.normal(size=128)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (128,), torch.from_numpy(w), torch.from_numpy(b),
+                                         eps=1e-5).numpy()
+    assert np.allclose(ops.layernorm(x, 1e-5, w, b), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_qk_layernorm_is_per_head():
+    """Each head is normalised on its own: scaling one head leaves the others."""
+    rng = np.random.default_rng(8)
+    u = rng.normal(size=(2, 3, 16))
+    w, b = rng.normal(size=16), rng.normal(size=16)
+    y = ops.qk_layernorm_per_head(u, w, b, 1e-6)
+    u2 = u.copy()
+    u2[:, 1] *= 10
+    y2 = ops.qk_layernorm_per_head(u2, w, b, 1e-6)
+    assert np.allclose(y[:, [0, 2]], y2[:, [0, 2]], rtol=0, atol=0)
+    assert np.allclose(y[:, 1], y2[:, 1], atol=1e-6)      # only eps separates them
+
+
 def test_rope_worked_example():
     g = load("rope_worked.json")
     u = np.array(g["u"]).reshape(1, 1, 4)

@@ -98,9 +98,22 @@ def test_pi05_decoder_chain_180_calls(gbf):
     assert_bf16_close(to_bits(res_gpu), res_ref, "final residual")
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
-def test_large_sweep_shape_sampled_rows(gbf, mode):
-    """65536 x 4096 in the bench's launch configuration; the oracle checks 64 rows."""
-    c = workloads.add_rmsnorm_case(65536, 4096, mode, seed=11)
+@pytest.mark.parametrize("mode,gated", [(0, False), (1, False), (2, True), (2, False), (0, True)])
+def test_large_sweep_shape_sampled_rows(gbf, mode, gated):
+    """65536 x 4096 in the bench's launch configuration (two vectors per
+    thread; Ada reloads its factors every row); the oracle checks 64 rows."""
+    c = workloads.add_rmsnorm_case(65536, 4096, mode, seed=11, gated=gated)
     rows = np.sort(np.random.default_rng(0).choice(65536, 64, replace=False))
-    check(gbf, c, rows=rows, what=f"65536x4096 mode {mode}")
+    check(gbf, c, rows=rows, what=f"65536x4096 mode {mode} gated {gated}")
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("rows,hidden", [(20011, 1024), (10007, 1032), (2003, 8192)])
+def test_large_launch_plans_sampled_rows(gbf, mode, rows, hidden):
+    """Launches large enough for the multi-vector plans: two vectors per thread
+    with several rows per CTA and a ragged last CTA (1024), a vector count
+    that leaves lanes idle (1032), and four vectors per thread (8192); the
+    oracle checks the first, last and 62 random rows."""
+    c = workloads.add_rmsnorm_case(rows, hidden, mode, seed=rows + hidden + mode, gated=mode == 2)
+    pick = np.unique(np.concatenate([[0, rows - 1], np.random.default_rng(mode).choice(rows, 62, replace=False)]))
+    check(gbf, c, rows=pick, what=f"[{rows},{hidden}] mode {mode}")
