@@ -11,6 +11,7 @@ own seeded synthetic inputs already resident in HBM:
   sweep_ada            gated AdaRMSNorm + FP8 at [65536, 4096]
   qwen3_qkv            packed QKV [4096, 48*128], per-head norm, 1D RoPE; four calls on
                        four buffer sets (100 MB each, under the L2 size) back to back
+  chameleon_qkv_ln     packed QKV [4096, 96*128], per-head LayerNorm (weight + bias), 1D RoPE
   wan_qkv3d            packed QKV [32760, 3*5120], full-width norm, 3D RoPE
   linear_bias_gelu     X [8192, 4096] . W[16384, 4096]^T + b, GELU(tanh)
   bn_fold              W [16384, 4096], BN of its 16384 output channels
@@ -62,6 +63,11 @@ def bytes_qkv(tokens, hq, hkv, d, norm, rope):
     w = (2 * d if norm == 0 else (hq + hkv) * d) * 2
     pos = tokens * (3 if rope else 1) * 4
     return io + w + pos
+
+
+def bytes_qkv_layernorm(tokens, hq, hkv, d, biases=True):
+    """Per-head LayerNorm variant: the RMSNorm bytes plus the two bias vectors."""
+    return bytes_qkv(tokens, hq, hkv, d, 0, 0) + (2 * d * 2 if biases else 0)
 
 
 def bytes_unfused_add_rmsnorm(rows, hidden, mode):
@@ -231,6 +237,9 @@ class QkvOp(Op):
         t, hq, hkv, d = c["tokens"], c["n_q"], c["n_kv"], c["d"]
         qkv = from_bits(c["qkv"])
         self.qw, self.kw = from_bits(c["q_w"]), from_bits(c["k_w"])
+        self.ln = c["norm"] == 2            # per-head LayerNorm entry point
+        self.qb = None if c.get("q_b") is None else from_bits(c["q_b"])
+        self.kb = None if c.get("k_b") is None else from_bits(c["k_b"])
         self.pos = torch.from_numpy(np.ascontiguousarray(c["pos"])).cuda()
         self.sets = []
         for i in range(sets):
@@ -245,18 +254,25 @@ class QkvOp(Op):
     def run(self):
         c = self.c
         for qkv, qo, kc, vc in self.sets:
-            self.gbf.qkv_split_norm_rope(qkv, c["n_q"], c["n_kv"], c["d"], c["norm"], self.qw, self.kw, c["eps"],
-                                         c["rope"], self.pos, c["theta"], qo, kc, vc, sections=c["sections"])
+            if self.ln:
+                self.gbf.qkv_split_layernorm_rope(qkv, c["n_q"], c["n_kv"], c["d"], self.qw, self.qb, self.kw,
+                                                  self.kb, c["eps"], self.pos, c["theta"], qo, kc, vc)
+            else:
+                self.gbf.qkv_split_norm_rope(qkv, c["n_q"], c["n_kv"], c["d"], c["norm"], self.qw, self.kw,
+                                             c["eps"], c["rope"], self.pos, c["theta"], qo, kc, vc,
+                                             sections=c["sections"])
 
     def algorithmic_bytes(self):
         c = self.c
+        if self.ln:
+            return self.launches * bytes_qkv_layernorm(c["tokens"], c["n_q"], c["n_kv"], c["d"], self.qb is not None)
         return self.launches * bytes_qkv(c["tokens"], c["n_q"], c["n_kv"], c["d"], c["norm"], c["rope"])
 
     def unfused_bytes(self):
         c = self.c
         t, hq, hkv, d = c["tokens"], c["n_q"], c["n_kv"], c["d"]
         q, kv = t * hq * d * 2, t * hkv * d * 2
-        if c["norm"] == 0:   # views for the split; q norm+rope 4 passes, k norm+rope+cache 6, v cache 2
+        if c["norm"] in (0, 2):   # views for the split; q norm+rope 4 passes, k norm+rope+cache 6, v cache 2
             return self.launches * (4 * q + 6 * kv + 2 * kv)
         return self.launches * (6 * (q + 2 * kv) + 4 * (q + kv) + 4 * (q + kv))   # split, two norms, two ropes
 
@@ -264,7 +280,8 @@ class QkvOp(Op):
         return self.launches * self.c["tokens"]
 
     def e2e_buffers(self):
-        return [st[0] for st in self.sets] + [self.qw, self.kw, self.pos], [t for st in self.sets for t in st[1:]]
+        params = [t for t in (self.qw, self.kw, self.qb, self.kb, self.pos) if t is not None]
+        return [st[0] for st in self.sets] + params, [t for st in self.sets for t in st[1:]]
 
 
 class GemmOp(Op):
@@ -329,6 +346,7 @@ class FoldOp(Op):
 
 
 OP_NAMES = ("add_rmsnorm_fp8", "pi05_ada_chain", "sweep_weighted", "sweep_noweight", "sweep_ada", "qwen3_qkv",
+            "chameleon_qkv_ln",
             "wan_qkv3d", "linear_bias_gelu", "bn_fold")
 
 
@@ -349,6 +367,8 @@ def build_ops(gbf, with_gemm, only=None, small=False):
             ops.append(AddRmsNormOp(gbf, name, rows, 4096, mode, gated, seed))
     if "qwen3_qkv" in want:       # 100 MB per call, under the L2 size: four buffer sets
         ops.append(QkvOp(gbf, "qwen3_qkv", workloads.config_qwen3_qkv(), sets=1 if small else 4))
+    if "chameleon_qkv_ln" in want:
+        ops.append(QkvOp(gbf, "chameleon_qkv_ln", workloads.config_chameleon_qkv(tokens=2048 if small else 4096)))
     if "wan_qkv3d" in want:
         ops.append(QkvOp(gbf, "wan_qkv3d", workloads.config_wan_qkv(tokens=4096 if small else None)))
     if want & {"linear_bias_gelu", "bn_fold"}:
@@ -491,6 +511,7 @@ def kernel_source_hash(source):
 KERNEL_FILE = {"add_rmsnorm_fp8": "add_rmsnorm_fp8.cu", "pi05_ada_chain": "add_rmsnorm_fp8.cu",
                "sweep_weighted": "add_rmsnorm_fp8.cu", "sweep_noweight": "add_rmsnorm_fp8.cu",
                "sweep_ada": "add_rmsnorm_fp8.cu", "qwen3_qkv": "qkv_norm_rope.cu", "wan_qkv3d": "qkv_norm_rope.cu",
+               "chameleon_qkv_ln": "qkv_norm_rope.cu",
                "linear_bias_gelu": "gemm_tcgen05.cu", "bn_fold": "bn_fold.cu"}
 
 
@@ -538,6 +559,11 @@ def cpu_baseline_sample(scale=1):
     dt = timed(lambda: chains.qkv_split_norm_rope(c["qkv"], 32, 8, 128, 0, c["q_w"], c["k_w"], c["eps"], 0, c["pos"],
                                                   c["theta"]))
     res["qwen3_qkv"] = (bytes_qkv(tq, 32, 8, 128, 0, 0), dt)
+    tc = 128 * scale
+    c = workloads.config_chameleon_qkv(tokens=tc)
+    dt = timed(lambda: chains.qkv_split_norm_rope(c["qkv"], 32, 32, 128, chains.QKNORM_LAYERNORM, c["q_w"], c["k_w"],
+                                                  c["eps"], 0, c["pos"], c["theta"], q_b=c["q_b"], k_b=c["k_b"]))
+    res["chameleon_qkv_ln"] = (bytes_qkv_layernorm(tc, 32, 32, 128), dt)
     tw = 64 * scale
     c = workloads.config_wan_qkv(tokens=tw)
     dt = timed(lambda: chains.qkv_split_norm_rope(c["qkv"], 40, 40, 128, 1, c["q_w"], c["k_w"], c["eps"], 1,
@@ -571,7 +597,8 @@ def run_cpu_baseline(scale=32):
     return {"value": round(d["gbs"], 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": (f"float64 numpy oracle, one thread: [16,256] add+RMSNorm+FP8; {min(10 * scale, 180)} of the 180 "
                        f"chained [10,1024] AdaRMSNorm calls; {64 * scale} rows of each [65536,4096] sweep; "
-                       f"{256 * scale} Qwen3 tokens; {64 * scale} Wan tokens; BN fold of {1024 * scale} channels; "
+                       f"{256 * scale} Qwen3 tokens; {128 * scale} Chameleon tokens; {64 * scale} Wan tokens; "
+                       f"BN fold of {1024 * scale} channels; "
                        "GB/s = algorithmic bytes / oracle time over the memory-bound operators (a "
                        f"{16 * scale}-row sample of the GEMM is in per_op as GFLOP/s)"),
             "seconds": round(d["seconds"], 3), "per_op": d["per_op"]}

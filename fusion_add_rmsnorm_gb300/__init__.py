@@ -36,6 +36,8 @@ _SIGNATURES = {
     "gbf_add_rmsnorm_fp8": [_p, _p, _p, _p, _i32, _p, _p, _p, _p, _i64, _i64, _f, _f, _p],
     "gbf_qkv_split_norm_rope": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _f, _i32, _p, _p, _f, _p, _p, _p,
                                 _p, _i64, _p],
+    "gbf_qkv_split_layernorm_rope": [_p, _i64, _i32, _i32, _i32, _p, _p, _p, _p, _f, _p, _f, _p, _p, _p, _p, _i64,
+                                     _p],
     "gbf_linear_bias_gelu": [_p, _p, _p, _p, _i64, _i64, _i64, _i32, _p],
     "gbf_bn_fold": [_p, _p, _p, _p, _p, _p, _f, _i64, _i64, _p, _p, _p],
     "gbf_copy": [_p, _p, _i64, _p],
@@ -103,6 +105,17 @@ def qkv_split_norm_rope(qkv, n_q_heads, n_kv_heads, head_dim, norm, q_w, k_w, ep
                                                ctypes.cast(sec, ctypes.c_void_p) if sec is not None else None,
                                                theta, _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(slots),
                                                rows, _stream(stream)))
+
+
+def qkv_split_layernorm_rope(qkv, n_q_heads, n_kv_heads, head_dim, q_w, q_b, k_w, k_b, eps, pos, theta, q_out,
+                             k_cache, v_cache, slots=None, cache_rows=None, stream=None):
+    """gbf_qkv_split_layernorm_rope: per-head LayerNorm (biases may be None) + 1D RoPE."""
+    tokens = qkv.shape[0]
+    rows = k_cache.shape[0] if cache_rows is None else cache_rows
+    return _check(_lib.gbf_qkv_split_layernorm_rope(_ptr(qkv), tokens, n_q_heads, n_kv_heads, head_dim, _ptr(q_w),
+                                                    _ptr(q_b), _ptr(k_w), _ptr(k_b), eps, _ptr(pos), theta,
+                                                    _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(slots), rows,
+                                                    _stream(stream)))
 
 
 def linear_bias_gelu(x, w, bias, y, act=ACT_GELU_TANH, stream=None):

@@ -132,15 +132,17 @@ GBF_API int gbf_add_rmsnorm_fp8(const void* x, const void* res_in, void* res_out
 
 // --------------------------------------------- packed QKV split + norm + RoPE
 
-GBF_API int gbf_qkv_split_norm_rope(const void* qkv, int64_t tokens, int n_q_heads, int n_kv_heads, int head_dim,
-                                    int norm, const void* q_w, const void* k_w, float eps, int rope,
-                                    const int32_t* pos, const int32_t* sections, float theta, void* q_out,
-                                    void* k_cache, void* v_cache, const int32_t* slots, int64_t cache_rows,
-                                    void* stream) {
-  const char* fn = "gbf_qkv_split_norm_rope";
+namespace {
+
+// Both QKV entry points: norm is GBF_QKNORM_PER_HEAD / FULL_WIDTH (RMSNorm, no
+// biases) or kQkNormLayerNorm (per-head LayerNorm with optional biases).
+int qkv_entry(const char* fn, const void* qkv, int64_t tokens, int n_q_heads, int n_kv_heads, int head_dim,
+              int norm, const void* q_w, const void* q_b, const void* k_w, const void* k_b, float eps, int rope,
+              const int32_t* pos, const int32_t* sections, float theta, void* q_out, void* k_cache, void* v_cache,
+              const int32_t* slots, int64_t cache_rows, void* stream) {
   if (tokens < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0)
     return fail(GBF_EINVAL, "%s: tokens >= 0 and positive head counts / head_dim are required", fn);
-  if (norm != GBF_QKNORM_PER_HEAD && norm != GBF_QKNORM_FULL_WIDTH)
+  if (norm != GBF_QKNORM_PER_HEAD && norm != GBF_QKNORM_FULL_WIDTH && norm != gbf::kQkNormLayerNorm)
     return fail(GBF_EINVAL, "%s: unknown norm %d", fn, norm);
   if (rope != GBF_ROPE_1D && rope != GBF_ROPE_3D) return fail(GBF_EINVAL, "%s: unknown rope %d", fn, rope);
   if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(GBF_EINVAL, "%s: eps must be finite and >= 0", fn);
@@ -149,6 +151,8 @@ GBF_API int gbf_qkv_split_norm_rope(const void* qkv, int64_t tokens, int n_q_hea
     return fail(GBF_EUNSUPPORTED, "%s: head_dim (%d) must be a multiple of 16 and <= 256", fn, head_dim);
   if (norm == GBF_QKNORM_PER_HEAD && (head_dim & (head_dim - 1)) != 0)
     return fail(GBF_EUNSUPPORTED, "%s: per-head norm needs a power-of-two head_dim (got %d)", fn, head_dim);
+  if (norm == gbf::kQkNormLayerNorm && !gbf::qkv_uses_rot1d(norm, rope, head_dim))
+    return fail(GBF_EUNSUPPORTED, "%s: LayerNorm needs 1D RoPE and head_dim 64, 128 or 256 (got %d)", fn, head_dim);
   if (n_q_heads > 4096 || n_kv_heads > 4096) return fail(GBF_EUNSUPPORTED, "%s: too many heads", fn);
   if (!gbf::qkv_uses_rot1d(norm, rope, head_dim) &&
       (6LL * n_q_heads + 8LL * n_kv_heads) * head_dim > gbf::kQkvStagedMaxBytes)
@@ -174,20 +178,22 @@ GBF_API int gbf_qkv_split_norm_rope(const void* qkv, int64_t tokens, int n_q_hea
   if (!qkv || !q_w || !k_w || !pos || !q_out || !k_cache || !v_cache)
     return fail(GBF_EINVAL, "%s: qkv, q_w, k_w, pos, q_out, k_cache, v_cache are required", fn);
   const void* al[] = {qkv, q_w, k_w, q_out, k_cache, v_cache};
+  if ((q_b && reinterpret_cast<uintptr_t>(q_b) % 16) || (k_b && reinterpret_cast<uintptr_t>(k_b) % 16))
+    return fail(GBF_EALIGN, "%s: biases must be 16-byte aligned", fn);
   for (const void* p : al)
     if (!aligned16(p)) return fail(GBF_EALIGN, "%s: tensors must be 16-byte aligned", fn);
   const int64_t D = head_dim;
   const int64_t in_b = tokens * (n_q_heads + 2LL * n_kv_heads) * D * 2;
-  const int64_t wq_b = (norm == GBF_QKNORM_PER_HEAD ? D : n_q_heads * D) * 2;
-  const int64_t wk_b = (norm == GBF_QKNORM_PER_HEAD ? D : n_kv_heads * D) * 2;
+  const int64_t wq_b = (norm == GBF_QKNORM_FULL_WIDTH ? n_q_heads * D : D) * 2;
+  const int64_t wk_b = (norm == GBF_QKNORM_FULL_WIDTH ? n_kv_heads * D : D) * 2;
   const int64_t pos_b = tokens * (rope == GBF_ROPE_3D ? 3 : 1) * 4;
-  const int64_t q_b = tokens * n_q_heads * D * 2, c_b = cache_rows * n_kv_heads * D * 2;
+  const int64_t qo_b = tokens * n_q_heads * D * 2, c_b = cache_rows * n_kv_heads * D * 2;
   void* outs[] = {q_out, k_cache, v_cache};
-  const int64_t out_len[] = {q_b, c_b, c_b};
-  const void* ins[] = {qkv, q_w, k_w, pos, slots};
-  const int64_t in_len[] = {in_b, wq_b, wk_b, pos_b, slots ? tokens * 4 : 0};
+  const int64_t out_len[] = {qo_b, c_b, c_b};
+  const void* ins[] = {qkv, q_w, k_w, pos, slots, q_b, k_b};
+  const int64_t in_len[] = {in_b, wq_b, wk_b, pos_b, slots ? tokens * 4 : 0, q_b ? D * 2 : 0, k_b ? D * 2 : 0};
   for (int i = 0; i < 3; ++i) {
-    for (int j = 0; j < 5; ++j)
+    for (int j = 0; j < 7; ++j)
       if (overlap(outs[i], out_len[i], ins[j], in_len[j])) return fail(GBF_EINVAL, "%s: an output overlaps an input", fn);
     for (int j = i + 1; j < 3; ++j)
       if (overlap(outs[i], out_len[i], outs[j], out_len[j])) return fail(GBF_EINVAL, "%s: outputs overlap", fn);
@@ -197,6 +203,8 @@ GBF_API int gbf_qkv_split_norm_rope(const void* qkv, int64_t tokens, int n_q_hea
   a.qkv = qkv;
   a.q_w = q_w;
   a.k_w = k_w;
+  a.q_b = q_b;
+  a.k_b = k_b;
   a.pos = pos;
   a.slots = slots;
   a.q_out = q_out;
@@ -229,6 +237,30 @@ GBF_API int gbf_qkv_split_norm_rope(const void* qkv, int64_t tokens, int n_q_hea
     start += w;
   }
   return launch_status(gbf::launch_qkv_split_norm_rope(a, static_cast<cudaStream_t>(stream)), fn);
+}
+
+}  // namespace
+
+GBF_API int gbf_qkv_split_norm_rope(const void* qkv, int64_t tokens, int n_q_heads, int n_kv_heads, int head_dim,
+                                    int norm, const void* q_w, const void* k_w, float eps, int rope,
+                                    const int32_t* pos, const int32_t* sections, float theta, void* q_out,
+                                    void* k_cache, void* v_cache, const int32_t* slots, int64_t cache_rows,
+                                    void* stream) {
+  const char* fn = "gbf_qkv_split_norm_rope";
+  if (norm != GBF_QKNORM_PER_HEAD && norm != GBF_QKNORM_FULL_WIDTH)
+    return fail(GBF_EINVAL, "%s: unknown norm %d", fn, norm);
+  return qkv_entry(fn, qkv, tokens, n_q_heads, n_kv_heads, head_dim, norm, q_w, nullptr, k_w, nullptr, eps, rope,
+                   pos, sections, theta, q_out, k_cache, v_cache, slots, cache_rows, stream);
+}
+
+GBF_API int gbf_qkv_split_layernorm_rope(const void* qkv, int64_t tokens, int n_q_heads, int n_kv_heads,
+                                         int head_dim, const void* q_w, const void* q_b, const void* k_w,
+                                         const void* k_b, float eps, const int32_t* pos, float theta, void* q_out,
+                                         void* k_cache, void* v_cache, const int32_t* slots, int64_t cache_rows,
+                                         void* stream) {
+  return qkv_entry("gbf_qkv_split_layernorm_rope", qkv, tokens, n_q_heads, n_kv_heads, head_dim,
+                   gbf::kQkNormLayerNorm, q_w, q_b, k_w, k_b, eps, GBF_ROPE_1D, pos, nullptr, theta, q_out, k_cache,
+                   v_cache, slots, cache_rows, stream);
 }
 
 // ------------------------------------------------ Linear + bias + GELU GEMM

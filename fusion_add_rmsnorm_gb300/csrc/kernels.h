@@ -8,7 +8,7 @@
 namespace gbf {
 
 enum { kNormWeight = 0, kNormNoWeight = 1, kNormAda = 2 };
-enum { kQkNormPerHead = 0, kQkNormFullWidth = 1 };
+enum { kQkNormPerHead = 0, kQkNormFullWidth = 1, kQkNormLayerNorm = 2 };
 enum { kRope1D = 0, kRope3D = 1 };
 enum { kActNone = 0, kActGeluTanh = 1 };
 
@@ -47,6 +47,8 @@ struct QkvArgs {
   const void* qkv;
   const void* q_w;
   const void* k_w;
+  const void* q_b;        // LayerNorm biases (nullable: 0)
+  const void* k_b;
   const int32_t* pos;
   const int32_t* slots;   // nullable
   void* q_out;

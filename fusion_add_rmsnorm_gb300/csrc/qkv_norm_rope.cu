@@ -88,7 +88,7 @@ constexpr int kRotGroups = 16;              // head groups per token
 constexpr int kRotBlock = 256;
 constexpr int kRotBatch = 3;                // heads whose loads are in flight together
 
-template <int LPH>
+template <int LPH, bool LN>
 __global__ void __launch_bounds__(kRotBlock, 4)
 qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   constexpr int D = LPH * 16;
@@ -168,36 +168,92 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
           }
           const uint32_t xl[4] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w};
           const uint32_t xh[4] = {hi[u].x, hi[u].y, hi[u].z, hi[u].w};
-          float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            s0 = fma_bf16_lo(xl[i], xl[i], s0);
-            s1 = fma_bf16_hi(xl[i], xl[i], s1);
-            s0 = fma_bf16_lo(xh[i], xh[i], s0);
-            s1 = fma_bf16_hi(xh[i], xh[i], s1);
-          }
-          const float ss = segment_sum(s0 + s1, LPH);   // the head's LPH lanes only
-          const bool is_q = h < a.n_q;
-          if (!is_q && !slot_ok) continue;
-          const float inv = rsqrtf(ss / static_cast<float>(D) + a.eps);
-          const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(is_q ? a.q_w : a.k_w);
-          const uint4 wlv = ld_cached(w + lane * 8), whv = ld_cached(w + (lane + LPH) * 8);
-          const uint32_t wl[4] = {wlv.x, wlv.y, wlv.z, wlv.w};
-          const uint32_t wh[4] = {whv.x, whv.y, whv.z, whv.w};
           uint32_t ol[4], oh[4];
+          if (!LN) {
+            // RMSNorm: o = rotate(x * w) * inv
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            // pair (8 lane + 2i + j, the same + D/2) for j = 0, 1 in the two float2 lanes
-            const float2 ul = make_float2(fma_bf16_lo(xl[i], wl[i], 0.f), fma_bf16_hi(xl[i], wl[i], 0.f));
-            const float2 uh = make_float2(fma_bf16_lo(xh[i], wh[i], 0.f), fma_bf16_hi(xh[i], wh[i], 0.f));
-            float2 rl, rh;
-            rl.x = fmaf(ul.x, c2[i].x, -(s2[i].x * uh.x)) * inv;
-            rl.y = fmaf(ul.y, c2[i].y, -(s2[i].y * uh.y)) * inv;
-            rh.x = fmaf(uh.x, c2[i].x, s2[i].x * ul.x) * inv;
-            rh.y = fmaf(uh.y, c2[i].y, s2[i].y * ul.y) * inv;
-            ol[i] = f32x2_to_bf16x2(rl.x, rl.y);
-            oh[i] = f32x2_to_bf16x2(rh.x, rh.y);
+            for (int i = 0; i < 4; ++i) {
+              s0 = fma_bf16_lo(xl[i], xl[i], s0);
+              s1 = fma_bf16_hi(xl[i], xl[i], s1);
+              s0 = fma_bf16_lo(xh[i], xh[i], s0);
+              s1 = fma_bf16_hi(xh[i], xh[i], s1);
+            }
+            const float ss = segment_sum(s0 + s1, LPH);   // the head's LPH lanes only
+            const bool is_q = h < a.n_q;
+            if (!is_q && !slot_ok) continue;
+            const float inv = rsqrtf(ss / static_cast<float>(D) + a.eps);
+            const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(is_q ? a.q_w : a.k_w);
+            const uint4 wlv = ld_cached(w + lane * 8), whv = ld_cached(w + (lane + LPH) * 8);
+            const uint32_t wl[4] = {wlv.x, wlv.y, wlv.z, wlv.w};
+            const uint32_t wh[4] = {whv.x, whv.y, whv.z, whv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              // pair (8 lane + 2i + j, the same + D/2) for j = 0, 1 in the two float2 lanes
+              const float2 ul = make_float2(fma_bf16_lo(xl[i], wl[i], 0.f), fma_bf16_hi(xl[i], wl[i], 0.f));
+              const float2 uh = make_float2(fma_bf16_lo(xh[i], wh[i], 0.f), fma_bf16_hi(xh[i], wh[i], 0.f));
+              float2 rl, rh;
+              rl.x = fmaf(ul.x, c2[i].x, -(s2[i].x * uh.x)) * inv;
+              rl.y = fmaf(ul.y, c2[i].y, -(s2[i].y * uh.y)) * inv;
+              rh.x = fmaf(uh.x, c2[i].x, s2[i].x * ul.x) * inv;
+              rh.y = fmaf(uh.y, c2[i].y, s2[i].y * ul.y) * inv;
+              ol[i] = f32x2_to_bf16x2(rl.x, rl.y);
+              oh[i] = f32x2_to_bf16x2(rh.x, rh.y);
+            }
+          } else {
+            // LayerNorm, two passes over the registers: mean, then centred
+            // squares; u = (x - mean) * inv * w + b, o = rotate(u)
+            float xf_l[8], xf_h[8];
+            bf16x8_to_f32(lo[u], xf_l);
+            bf16x8_to_f32(hi[u], xf_h);
+            float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              m0 += xf_l[i];
+              m1 += xf_h[i];
+            }
+            const float mean = segment_sum(m0 + m1, LPH) * (1.0f / static_cast<float>(D));
+            float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              xf_l[i] -= mean;
+              xf_h[i] -= mean;
+              v0 = fmaf(xf_l[i], xf_l[i], v0);
+              v1 = fmaf(xf_h[i], xf_h[i], v1);
+            }
+            const float var = segment_sum(v0 + v1, LPH) * (1.0f / static_cast<float>(D));
+            const bool is_q = h < a.n_q;
+            if (!is_q && !slot_ok) continue;
+            const float inv = rsqrtf(var + a.eps);
+            const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(is_q ? a.q_w : a.k_w);
+            const __nv_bfloat16* bb = static_cast<const __nv_bfloat16*>(is_q ? a.q_b : a.k_b);
+            float wl[8], wh[8], bl[8], bh[8];
+            bf16x8_to_f32(ld_cached(w + lane * 8), wl);
+            bf16x8_to_f32(ld_cached(w + (lane + LPH) * 8), wh);
+            if (bb) {
+              bf16x8_to_f32(ld_cached(bb + lane * 8), bl);
+              bf16x8_to_f32(ld_cached(bb + (lane + LPH) * 8), bh);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) bl[i] = bh[i] = 0.f;
+            }
+            float rl[8], rh[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float ul = fmaf(xf_l[i] * inv, wl[i], bl[i]);
+              const float uh = fmaf(xf_h[i] * inv, wh[i], bh[i]);
+              const float c = (i & 1) ? c2[i >> 1].y : c2[i >> 1].x;
+              const float sn = (i & 1) ? s2[i >> 1].y : s2[i >> 1].x;
+              rl[i] = fmaf(ul, c, -(sn * uh));
+              rh[i] = fmaf(uh, c, sn * ul);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              ol[i] = f32x2_to_bf16x2(rl[2 * i], rl[2 * i + 1]);
+              oh[i] = f32x2_to_bf16x2(rh[2 * i], rh[2 * i + 1]);
+            }
           }
+          const bool is_q = h < a.n_q;
           __nv_bfloat16* dst = is_q ? static_cast<__nv_bfloat16*>(a.q_out) + (t * a.n_q + h) * D
                                     : static_cast<__nv_bfloat16*>(a.k_cache) + (crow * a.n_kv + (h - a.n_q)) * D;
           st_16(dst + lane * 8, make_uint4(ol[0], ol[1], ol[2], ol[3]));
@@ -611,13 +667,15 @@ template <int LPH>
 cudaError_t launch_rot1d(const QkvArgs& a, cudaStream_t stream) {
   const int tok_per_cta = kRotBlock / (kRotGroups * LPH);
   const unsigned grid = static_cast<unsigned>((a.tokens + tok_per_cta - 1) / tok_per_cta);
-  return launch_pdl(qkv_rot1d_kernel<LPH>, dim3(grid), dim3(kRotBlock), 0, stream, a);
+  if (a.norm == kQkNormLayerNorm)
+    return launch_pdl(qkv_rot1d_kernel<LPH, true>, dim3(grid), dim3(kRotBlock), 0, stream, a);
+  return launch_pdl(qkv_rot1d_kernel<LPH, false>, dim3(grid), dim3(kRotBlock), 0, stream, a);
 }
 
 }  // namespace
 
 bool qkv_uses_rot1d(int norm, int rope, int d) {
-  return norm == kQkNormPerHead && rope == kRope1D && (d == 64 || d == 128 || d == 256);
+  return (norm == kQkNormPerHead || norm == kQkNormLayerNorm) && rope == kRope1D && (d == 64 || d == 128 || d == 256);
 }
 
 cudaError_t launch_qkv_split_norm_rope(const QkvArgs& a, cudaStream_t stream) {

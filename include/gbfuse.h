@@ -130,6 +130,28 @@ GBF_API int gbf_qkv_split_norm_rope(const void* qkv, int64_t tokens, int n_q_hea
                                     int64_t cache_rows, void* stream);
 
 /*
+ * gbf_qkv_split_layernorm_rope -- the same single pass as
+ * gbf_qkv_split_norm_rope with a per-head LayerNorm in place of the RMSNorm:
+ * FlashRT §2.2 (Chameleon prefill: LayerNorm(Q) + LayerNorm(K) + two
+ * rotate_half RoPEs in one kernel, each lane holding both members of its
+ * rotation pairs).
+ *
+ * Per head of width head_dim: mean = Σx / D, var = Σ(x - mean)² / D,
+ * u = (x - mean) / sqrt(var + eps) * w + b in float32, then 1D rotate_half
+ * RoPE by pos[t] * theta^(-2j/head_dim) exactly as gbf_qkv_split_norm_rope.
+ * q_w, k_w: device bf16 [head_dim]; q_b, k_b: device bf16 [head_dim] or NULL
+ * (zero bias).  All other arguments, layouts, the V copy, slots and the device
+ * error word are those of gbf_qkv_split_norm_rope with norm per head and
+ * rope 1D.  Requires head_dim 64, 128 or 256 (GBF_EUNSUPPORTED otherwise);
+ * 16-byte aligned tensors including the biases; eps >= 0; theta > 0.
+ */
+GBF_API int gbf_qkv_split_layernorm_rope(const void* qkv, int64_t tokens, int n_q_heads, int n_kv_heads,
+                                         int head_dim, const void* q_w, const void* q_b, const void* k_w,
+                                         const void* k_b, float eps, const int32_t* pos, float theta, void* q_out,
+                                         void* k_cache, void* v_cache, const int32_t* slots, int64_t cache_rows,
+                                         void* stream);
+
+/*
  * gbf_linear_bias_gelu -- Y = act(X W^T + bias) on the tcgen05 tensor cores,
  * float32 accumulation in tensor memory, bias and GELU applied to the
  * accumulator tile before the single bf16 store.  OpenPPL §4.3 (epilogue:

@@ -26,7 +26,8 @@ def gbf():
 
 
 def test_header_declares_the_entry_points():
-    assert declared_symbols() == sorted(["gbf_add_rmsnorm_fp8", "gbf_qkv_split_norm_rope", "gbf_linear_bias_gelu",
+    assert declared_symbols() == sorted(["gbf_add_rmsnorm_fp8", "gbf_qkv_split_norm_rope",
+                                         "gbf_qkv_split_layernorm_rope", "gbf_linear_bias_gelu",
                                          "gbf_bn_fold", "gbf_copy", "gbf_device_status", "gbf_last_error",
                                          "gbf_version", "gbf_selftest_bounded_wait"])
 
@@ -109,6 +110,25 @@ def test_qkv_validation(gbf):
     assert call(norm=1, hq=220, hkv=40) == gbf.EUNSUPPORTED  # (6*220 + 8*40) * 128 > 196608
     assert call(norm=0, hq=220, hkv=40, tokens=0) == gbf.OK
     assert call(norm=1, hq=220, hkv=40, tokens=0) == gbf.EUNSUPPORTED
+
+
+def test_qkv_layernorm_validation(gbf):
+    L = gbf.raw()
+    call = lambda **k: L.gbf_qkv_split_layernorm_rope(*[k.get(n, d) for n, d in [       # noqa: E731
+        ("qkv", A(0)), ("tokens", 4), ("hq", 2), ("hkv", 1), ("d", 128), ("qw", A(1)), ("qb", A(7)),
+        ("kw", A(2)), ("kb", A(8)), ("eps", 1e-5), ("pos", A(3)), ("theta", 1e4),
+        ("q", A(4)), ("k", A(5)), ("v", A(6)), ("slots", None), ("rows", 4), ("stream", None)]])
+    assert call(tokens=0) == gbf.OK
+    assert call(tokens=0, qb=None, kb=None) == gbf.OK
+    assert call(d=96) == gbf.EUNSUPPORTED                    # only 64, 128, 256
+    assert call(d=512) == gbf.EUNSUPPORTED
+    assert call(eps=-1.0) == gbf.EINVAL
+    assert call(qw=None) == gbf.EINVAL
+    assert call(qb=ctypes.c_void_p(7 * F + 2)) == gbf.EALIGN
+    assert call(q=A(7)) == gbf.EINVAL                       # Q overlaps the Q bias
+    # the RMSNorm entry point does not take the LayerNorm mode
+    assert L.gbf_qkv_split_norm_rope(A(0), 4, 2, 1, 128, 2, A(1), A(2), ctypes.c_float(1e-6), 0, A(3), None,
+                                     ctypes.c_float(1e4), A(4), A(5), A(6), None, 4, None) == gbf.EINVAL
 
 
 def test_linear_and_fold_and_copy_validation(gbf):

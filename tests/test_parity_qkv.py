@@ -152,3 +152,79 @@ def test_out_of_range_slot_is_skipped_and_reported(gbf, norm, rope):
     assert_bf16_close(kc[slots[good]], rk[slots[good]], "K")
     assert not kc[3].any() and not vc[3].any()
     assert gbf.device_status()[0] == gbf.OK      # cleared by the read
+
+
+# ------------------------------------------------ per-head LayerNorm (Chameleon)
+
+def run_gpu_ln(gbf, c, slots=None, cache_rows=None):
+    t, hq, hkv, d = c["tokens"], c["n_q"], c["n_kv"], c["d"]
+    rows = t if cache_rows is None else cache_rows
+    q = torch.empty(t, hq, d, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(rows, hkv, d, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros(rows, hkv, d, dtype=torch.bfloat16, device="cuda")
+    pos = torch.from_numpy(np.ascontiguousarray(c["pos"])).cuda()
+    sl = None if slots is None else torch.from_numpy(np.asarray(slots, np.int32)).cuda()
+    opt = lambda k: None if c[k] is None else from_bits(c[k])      # noqa: E731
+    gbf.qkv_split_layernorm_rope(from_bits(c["qkv"]), hq, hkv, d, from_bits(c["q_w"]), opt("q_b"),
+                                 from_bits(c["k_w"]), opt("k_b"), c["eps"], pos, c["theta"], q, kc, vc, slots=sl,
+                                 cache_rows=rows)
+    torch.cuda.synchronize()
+    return to_bits(q), to_bits(kc), to_bits(vc)
+
+
+def run_oracle_ln(c, tok=None, slots=None, cache_rows=None):
+    sel = slice(None) if tok is None else tok
+    return chains.qkv_split_norm_rope(c["qkv"][sel], c["n_q"], c["n_kv"], c["d"], chains.QKNORM_LAYERNORM,
+                                      c["q_w"], c["k_w"], c["eps"], 0, c["pos"][sel], c["theta"], slots=slots,
+                                      cache_rows=cache_rows, q_b=c["q_b"], k_b=c["k_b"])
+
+
+def check_ln(gbf, c, what):
+    q, kc, vc = run_gpu_ln(gbf, c)
+    rq, rk, rv = run_oracle_ln(c)
+    assert_bf16_close(q, rq, what + " Q")
+    assert_bf16_close(kc, rk, what + " K")
+    assert np.array_equal(vc, rv), what + " V must be copied bit for bit"
+
+
+def test_chameleon_config_full(gbf):
+    """Packed [4096, 96*128], per-head LayerNorm with weight and bias on Q and
+    K, 1D RoPE theta 1e4 at positions 0..4095."""
+    check_ln(gbf, workloads.config_chameleon_qkv(), "chameleon")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("biases", [True, False])
+@pytest.mark.parametrize("tokens,hq,hkv", [(1, 1, 1), (13, 4, 2), (9, 3, 3), (37, 8, 1)])
+def test_layernorm_shapes(gbf, d, biases, tokens, hq, hkv):
+    c = workloads.layernorm_qkv_case(tokens, hq, hkv, d, seed=tokens + d + 7 * hq, biases=biases)
+    check_ln(gbf, c, f"LN d {d} biases {biases} [{tokens},{hq},{hkv}]")
+
+
+def test_layernorm_of_constant_heads_is_the_bias(gbf):
+    """Every Q and K head constant: the LayerNorm output is exactly the bias,
+    and at position 0 the rotation leaves it alone."""
+    c = workloads.layernorm_qkv_case(6, 4, 2, 128, seed=77)
+    t, width = c["tokens"], (4 + 4) * 128
+    vals = np.random.default_rng(0).normal(size=(t, 8, 1))
+    bits = torch.from_numpy(np.broadcast_to(vals, (t, 8, 128)).reshape(t, width).copy()).to(torch.bfloat16)
+    c["qkv"] = bits.view(torch.int16).numpy().view(np.uint16)
+    c["pos"] = np.zeros(t, np.int32)
+    q, kc, _ = run_gpu_ln(gbf, c)
+    assert np.array_equal(q, np.broadcast_to(c["q_b"], q.shape))
+    assert np.array_equal(kc, np.broadcast_to(c["k_b"], kc.shape))
+
+
+def test_layernorm_slots_and_out_of_range_slot(gbf):
+    c = workloads.layernorm_qkv_case(8, 2, 2, 128, seed=5)
+    gbf.device_status()
+    slots = np.array([3, 0, 7, 99, 4, 6, 1, 2], np.int32)
+    q, kc, vc = run_gpu_ln(gbf, c, slots=slots, cache_rows=10)
+    s, msg = gbf.device_status()
+    assert s == gbf.EDEVICE and "slot" in msg
+    good = slots != 99
+    rq, rk, rv = run_oracle_ln(c, tok=np.nonzero(good)[0], slots=slots[good], cache_rows=10)
+    assert_bf16_close(q, run_oracle_ln(c)[0], "Q is written for every token")
+    assert_bf16_close(kc[slots[good]], rk[slots[good]], "K")
+    assert np.array_equal(vc[slots[good]], rv[slots[good]])
+    assert not kc[[5, 8, 9]].any() and not vc[[5, 8, 9]].any()

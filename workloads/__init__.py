@@ -119,6 +119,26 @@ def config_qwen3_qkv(seed=0, tokens=4096):
     return qkv_case(tokens, 32, 8, 128, 0, 0, seed, theta=1e6)
 
 
+def layernorm_qkv_case(tokens, n_q_heads, n_kv_heads, head_dim, seed=0, theta=1e4, biases=True):
+    """Packed QKV bf16 [tokens, (Hq + 2 Hkv) * D] ~ N(0,1); then q_w, k_w =
+    1 + N(0, 0.1) and (when `biases`) q_b, k_b ~ N(0, 0.1), all [D]; eps 1e-5;
+    positions 0..tokens-1."""
+    c = qkv_case(tokens, n_q_heads, n_kv_heads, head_dim, 0, 0, seed, theta=theta)
+    d = Draw(seed + 1000)
+    c["norm"] = 2
+    c["eps"] = 1e-5
+    c["q_b"] = d.bf16_normal((head_dim,), std=0.1) if biases else None
+    c["k_b"] = d.bf16_normal((head_dim,), std=0.1) if biases else None
+    return c
+
+
+def config_chameleon_qkv(seed=0, tokens=4096):
+    """Chameleon-style prefill QKV post-processing (7B shapes): packed
+    [4096, (32+32+32)*128], per-head LayerNorm on Q and K with weight and
+    bias, rotate_half RoPE theta 1e4 at positions 0..4095."""
+    return layernorm_qkv_case(tokens, 32, 32, 128, seed, theta=1e4)
+
+
 WAN_GRID = (21, 30, 52)
 
 
