@@ -84,13 +84,16 @@ GBF_DEVICE int64_t cache_slot(const QkvArgs& a, int64_t t, bool& ok) {
 
 // --------------------------------------------------------- per-head, 1D
 
-constexpr int kRotGroups = 16;              // head groups per token
+// Head groups per token: a template parameter G of the per-head kernel,
+// chosen at launch so a thread has at most kRotBatch heads (one batch of
+// loads) where the token's 256 threads allow it.
 constexpr int kRotBlock = 256;
 constexpr int kRotBatch = 3;                // heads whose loads are in flight together
 
-template <int LPH, bool LN>
-__global__ void __launch_bounds__(kRotBlock, 4)
+template <int LPH, bool LN, int G>
+__global__ void __launch_bounds__(kRotBlock, LN ? 3 : 4)
 qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
+  constexpr int kRotGroups = G;
   constexpr int D = LPH * 16;
   constexpr int SLOTS = D / 2;
   constexpr int TPT = kRotGroups * LPH;     // threads per token
@@ -202,24 +205,27 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
             }
           } else {
             // LayerNorm, two passes over the registers: mean, then centred
-            // squares; u = (x - mean) * inv * w + b, o = rotate(u)
-            float xf_l[8], xf_h[8];
-            bf16x8_to_f32(lo[u], xf_l);
-            bf16x8_to_f32(hi[u], xf_h);
+            // squares; u = (x - mean) * inv * w + b, o = rotate(u).  The sums
+            // and the centring use the bf16-input FMA (x * 1 + acc, x * 1 - mean).
+            constexpr uint32_t kOnes = 0x3F803F80u;     // bf16x2 (1, 1)
             float m0 = 0.f, m1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              m0 += xf_l[i];
-              m1 += xf_h[i];
+            for (int i = 0; i < 4; ++i) {
+              m0 = fma_bf16_lo(xl[i], kOnes, m0);
+              m1 = fma_bf16_hi(xl[i], kOnes, m1);
+              m0 = fma_bf16_lo(xh[i], kOnes, m0);
+              m1 = fma_bf16_hi(xh[i], kOnes, m1);
             }
             const float mean = segment_sum(m0 + m1, LPH) * (1.0f / static_cast<float>(D));
-            float v0 = 0.f, v1 = 0.f;
+            float cl[8], ch[8], v0 = 0.f, v1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              xf_l[i] -= mean;
-              xf_h[i] -= mean;
-              v0 = fmaf(xf_l[i], xf_l[i], v0);
-              v1 = fmaf(xf_h[i], xf_h[i], v1);
+            for (int i = 0; i < 4; ++i) {
+              cl[2 * i] = fma_bf16_lo(xl[i], kOnes, -mean);
+              cl[2 * i + 1] = fma_bf16_hi(xl[i], kOnes, -mean);
+              ch[2 * i] = fma_bf16_lo(xh[i], kOnes, -mean);
+              ch[2 * i + 1] = fma_bf16_hi(xh[i], kOnes, -mean);
+              v0 = fmaf(cl[2 * i], cl[2 * i], fmaf(ch[2 * i], ch[2 * i], v0));
+              v1 = fmaf(cl[2 * i + 1], cl[2 * i + 1], fmaf(ch[2 * i + 1], ch[2 * i + 1], v1));
             }
             const float var = segment_sum(v0 + v1, LPH) * (1.0f / static_cast<float>(D));
             const bool is_q = h < a.n_q;
@@ -227,30 +233,22 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
             const float inv = rsqrtf(var + a.eps);
             const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(is_q ? a.q_w : a.k_w);
             const __nv_bfloat16* bb = static_cast<const __nv_bfloat16*>(is_q ? a.q_b : a.k_b);
-            float wl[8], wh[8], bl[8], bh[8];
-            bf16x8_to_f32(ld_cached(w + lane * 8), wl);
-            bf16x8_to_f32(ld_cached(w + (lane + LPH) * 8), wh);
-            if (bb) {
-              bf16x8_to_f32(ld_cached(bb + lane * 8), bl);
-              bf16x8_to_f32(ld_cached(bb + (lane + LPH) * 8), bh);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) bl[i] = bh[i] = 0.f;
-            }
-            float rl[8], rh[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float ul = fmaf(xf_l[i] * inv, wl[i], bl[i]);
-              const float uh = fmaf(xf_h[i] * inv, wh[i], bh[i]);
-              const float c = (i & 1) ? c2[i >> 1].y : c2[i >> 1].x;
-              const float sn = (i & 1) ? s2[i >> 1].y : s2[i >> 1].x;
-              rl[i] = fmaf(ul, c, -(sn * uh));
-              rh[i] = fmaf(uh, c, sn * ul);
-            }
+            const uint4 wlv = ld_cached(w + lane * 8), whv = ld_cached(w + (lane + LPH) * 8);
+            const uint4 blv = bb ? ld_cached(bb + lane * 8) : make_uint4(0, 0, 0, 0);
+            const uint4 bhv = bb ? ld_cached(bb + (lane + LPH) * 8) : make_uint4(0, 0, 0, 0);
+            const uint32_t wl[4] = {wlv.x, wlv.y, wlv.z, wlv.w}, wh[4] = {whv.x, whv.y, whv.z, whv.w};
+            const uint32_t bl[4] = {blv.x, blv.y, blv.z, blv.w}, bh[4] = {bhv.x, bhv.y, bhv.z, bhv.w};
+            // (lo, hi) halves of a packed bf16 pair as two floats
+            auto pair = [](uint32_t v) { return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u)); };
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              ol[i] = f32x2_to_bf16x2(rl[2 * i], rl[2 * i + 1]);
-              oh[i] = f32x2_to_bf16x2(rh[2 * i], rh[2 * i + 1]);
+              const float2 inv2 = make_float2(inv, inv);
+              const float2 ul = __ffma2_rn(__fmul2_rn(make_float2(cl[2 * i], cl[2 * i + 1]), inv2), pair(wl[i]), pair(bl[i]));
+              const float2 uh = __ffma2_rn(__fmul2_rn(make_float2(ch[2 * i], ch[2 * i + 1]), inv2), pair(wh[i]), pair(bh[i]));
+              const float2 rl = __ffma2_rn(ul, c2[i], __fmul2_rn(make_float2(-s2[i].x, -s2[i].y), uh));
+              const float2 rh = __ffma2_rn(uh, c2[i], __fmul2_rn(s2[i], ul));
+              ol[i] = f32x2_to_bf16x2(rl.x, rl.y);
+              oh[i] = f32x2_to_bf16x2(rh.x, rh.y);
             }
           }
           const bool is_q = h < a.n_q;
@@ -663,13 +661,27 @@ cudaError_t launch_staged(const QkvArgs& a, cudaStream_t stream) {
   return launch_pdl(qkv_staged_kernel<FULL>, dim3(grid), dim3(threads), smem, stream, b);
 }
 
-template <int LPH>
-cudaError_t launch_rot1d(const QkvArgs& a, cudaStream_t stream) {
-  const int tok_per_cta = kRotBlock / (kRotGroups * LPH);
+template <int LPH, int G>
+cudaError_t launch_rot1d_g(const QkvArgs& a, cudaStream_t stream) {
+  static_assert(G * LPH <= kRotBlock, "a token's threads fit one CTA");
+  const int tok_per_cta = kRotBlock / (G * LPH);
   const unsigned grid = static_cast<unsigned>((a.tokens + tok_per_cta - 1) / tok_per_cta);
   if (a.norm == kQkNormLayerNorm)
-    return launch_pdl(qkv_rot1d_kernel<LPH, true>, dim3(grid), dim3(kRotBlock), 0, stream, a);
-  return launch_pdl(qkv_rot1d_kernel<LPH, false>, dim3(grid), dim3(kRotBlock), 0, stream, a);
+    return launch_pdl(qkv_rot1d_kernel<LPH, true, G>, dim3(grid), dim3(kRotBlock), 0, stream, a);
+  return launch_pdl(qkv_rot1d_kernel<LPH, false, G>, dim3(grid), dim3(kRotBlock), 0, stream, a);
+}
+
+// G = the smallest of 8, 16, 32 head groups that leaves a thread at most
+// kRotBatch heads, within the 256 threads a token may use.
+template <int LPH>
+cudaError_t launch_rot1d(const QkvArgs& a, cudaStream_t stream) {
+  const int heads = a.n_q + 2 * a.n_kv;
+  const int gmax = kRotBlock / LPH > 32 ? 32 : kRotBlock / LPH;
+  int g = 8;
+  while (g < gmax && g * kRotBatch < heads) g *= 2;
+  if (g == 8) return launch_rot1d_g<LPH, 8>(a, stream);
+  if (g == 16) return launch_rot1d_g<LPH, 16>(a, stream);
+  return launch_rot1d_g<LPH, (LPH <= 8 ? 32 : 16)>(a, stream);
 }
 
 }  // namespace
