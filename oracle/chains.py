@@ -118,17 +118,30 @@ def qkv_split_norm_rope(qkv, n_q_heads, n_kv_heads, head_dim, norm, q_w, k_w, ep
     return q_out, k_cache, v_cache
 
 
-def linear_bias_gelu(x, w, bias=None, act_gelu=True):
+def linear_bias_gelu(x, w, bias=None, act_gelu=True, act=None):
     """Linear -> BiasAdd -> GELU(tanh) (OpenPPL §4.3 epilogue; Autofuse
     "MatMul -> BiasAdd -> ReLU" pattern with GELU; RFC §3.5 npu_linear).
 
     x: bf16 bits [M, K]; w: bf16 bits [N, K]; bias: bf16 bits [N] or None.
     The product is an exact-up-to-order float64 dot over K; the output is
-    rounded once to bf16."""
+    rounded once to bf16.  `act` (ops.ACT_*) selects another activation
+    (GELU erf, SiLU; RFC §3.6) in place of act_gelu's GELU(tanh)."""
     a = ops.linear(bf16_decode(x), bf16_decode(w), None if bias is None else bf16_decode(bias))
-    if act_gelu:
+    if act is not None:
+        a = ops.activation(a, act)
+    elif act_gelu:
         a = ops.gelu_tanh(a)
     return bf16_encode(a)
+
+
+def gated_act(x, d, act):
+    """Gated activation of a [rows, 2d] projection holding [gate | up]:
+    y = act(gate) * up, rounded once to bf16 (RFC §2.4 / §3.6: npu_swiglu
+    for SiLU, npu_gelu_mul for a GELU; two elementwise ops, one HBM pass).
+
+    x: bf16 bits [rows, 2d]; returns bf16 bits [rows, d]."""
+    v = bf16_decode(x).reshape(-1, 2 * d)
+    return bf16_encode(ops.gated_activation(v[:, :d], v[:, d:], act))
 
 
 def bn_fold_bf16(w, b, gamma, beta, mean, var, eps):

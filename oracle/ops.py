@@ -223,6 +223,43 @@ def gelu_tanh(a):
     return 0.5 * a * (1.0 + np.tanh(GELU_C0 * (a + GELU_C1 * a * a * a)))
 
 
+def gelu_erf(a):
+    """GELU, exact (erf) form: 0.5 a (1 + erf(a / sqrt(2))) -- the non-tanh
+    F.gelu that RFC §2.4 / §3.6 maps to npu_gelu.  erf is scipy's."""
+    from scipy.special import erf
+    a = np.asarray(a, np.float64)
+    return 0.5 * a * (1.0 + erf(a / np.sqrt(2.0)))
+
+
+def silu(a):
+    """SiLU a * sigmoid(a) = a / (1 + exp(-a)) (the gate of npu_swiglu, RFC
+    §2.4 / §3.6)."""
+    a = np.asarray(a, np.float64)
+    with np.errstate(over="ignore"):
+        return a / (1.0 + np.exp(-a))
+
+
+ACT_GELU_TANH, ACT_GELU_ERF, ACT_SILU = 1, 2, 3
+
+
+def activation(a, act):
+    """The activation selected by `act` (ACT_GELU_TANH / ACT_GELU_ERF / ACT_SILU)."""
+    if act == ACT_GELU_TANH:
+        return gelu_tanh(a)
+    if act == ACT_GELU_ERF:
+        return gelu_erf(a)
+    if act == ACT_SILU:
+        return silu(a)
+    raise ValueError(f"unknown activation {act}")
+
+
+def gated_activation(gate, up, act):
+    """act(gate) * up: SwiGLU with SiLU (npu_swiglu, vLLM's SiluAndMul),
+    GELU x Mul with a GELU (npu_gelu_mul: up_out * gelu(gate_out)); RFC §2.4,
+    §3.6."""
+    return activation(gate, act) * np.asarray(up, np.float64)
+
+
 # -------------------------------------------------------------- BatchNorm
 
 

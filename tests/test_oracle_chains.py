@@ -148,6 +148,24 @@ def test_qkv_layernorm_constant_heads_give_their_own_bias():
     assert not q0.any() and not k0.any()             # no bias: exactly zero
 
 
+def test_gated_act_splits_gate_then_up_and_rounds_once():
+    """The first half of each row is the gate, the second the up projection:
+    with up = 1 the output is bf16(act(gate)) and with gate = 1 it is
+    bf16(act(1) * up); rows are independent."""
+    rng = np.random.default_rng(41)
+    d = 8
+    gate = _rand_bits(rng, (3, d))
+    up = _rand_bits(rng, (3, d))
+    ones = bf16_encode(np.ones((3, d)))
+    for act in (ops.ACT_GELU_TANH, ops.ACT_GELU_ERF, ops.ACT_SILU):
+        y = chains.gated_act(np.concatenate([gate, ones], axis=1), d, act)
+        assert np.array_equal(y, bf16_encode(ops.activation(bf16_decode(gate), act)))
+        y = chains.gated_act(np.concatenate([ones, up], axis=1), d, act)
+        assert np.array_equal(y, bf16_encode(ops.activation(1.0, act) * bf16_decode(up)))
+    both = chains.gated_act(np.concatenate([gate, up], axis=1), d, ops.ACT_SILU)
+    assert np.array_equal(both[1:2], chains.gated_act(np.concatenate([gate, up], axis=1)[1:2], d, ops.ACT_SILU))
+
+
 def test_qkv_slots_permute_cache_rows():
     rng = np.random.default_rng(24)
     t, hq, hkv, d = 6, 2, 1, 8
@@ -191,6 +209,11 @@ def test_linear_bias_gelu_brute_force_tiny():
     y0 = chains.linear_bias_gelu(x, w, b, act_gelu=False)
     lib = torch.nn.functional.linear(torch.from_numpy(xv), torch.from_numpy(wv), torch.from_numpy(bv)).numpy()
     assert np.array_equal(y0, bf16_encode(lib))
+    # the other epilogue activations, against torch's fp64 ones on the same Linear
+    t = torch.from_numpy(lib)
+    for act, ref in ((ops.ACT_GELU_ERF, torch.nn.functional.gelu(t, approximate="none")),
+                     (ops.ACT_SILU, torch.nn.functional.silu(t))):
+        assert np.array_equal(chains.linear_bias_gelu(x, w, b, act=act), bf16_encode(ref.numpy()))
 
 
 def test_bn_fold_bf16_chain_worked_example():

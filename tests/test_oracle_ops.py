@@ -132,6 +132,43 @@ def test_qk_layernorm_is_per_head():
     assert np.allclose(y[:, 1], y2[:, 1], atol=1e-6)      # only eps separates them
 
 
+def test_gelu_erf_and_silu_match_torch_fp64():
+    torch = pytest.importorskip("torch")
+    a = np.linspace(-12, 12, 2001)
+    t = torch.from_numpy(a)
+    assert np.allclose(ops.gelu_erf(a), torch.nn.functional.gelu(t, approximate="none").numpy(), rtol=1e-14, atol=1e-15)
+    assert np.allclose(ops.silu(a), torch.nn.functional.silu(t).numpy(), rtol=1e-14, atol=1e-15)
+
+
+def test_gelu_erf_and_silu_closed_forms():
+    """f(a) - f(-a) = a for both (a (Phi(a) + Phi(-a)) = a, a (s(a) + s(-a)) = a);
+    f(0) = 0; f(a) -> a for large a and -> 0 for large -a; erf(1) and the
+    Gaussian CDF at 1 give GELU(1) = 0.841344746068543."""
+    a = np.linspace(-9, 9, 361)
+    for f in (ops.gelu_erf, ops.silu):
+        assert np.allclose(f(a) - f(-a), a, rtol=0, atol=1e-12)
+        assert f(0.0) == 0.0
+        assert abs(f(40.0) - 40.0) < 1e-12 and abs(f(-40.0)) < 1e-12
+    assert abs(ops.gelu_erf(1.0) - 0.841344746068543) < 1e-15
+    assert abs(ops.activation(1.0, ops.ACT_GELU_ERF) - 0.841344746068543) < 1e-15
+    assert ops.activation(2.0, ops.ACT_SILU) == ops.silu(2.0)
+    assert abs(ops.activation(1.0, ops.ACT_GELU_TANH) - 0.841344746068543) > 1e-4   # the tanh form differs
+    assert abs(ops.silu(1.0) - 1.0 / (1.0 + np.exp(-1.0))) == 0.0
+    assert np.all(np.isfinite(ops.silu(np.array([-1e4, 1e4]))))
+
+
+def test_gated_activation_is_gate_act_times_up():
+    """up = 1 gives act(gate); gate large gives up * gate; up = 0 gives 0;
+    GELU tanh and erf agree to the tanh form's 1e-3 approximation error."""
+    rng = np.random.default_rng(3)
+    g, u = rng.normal(size=64) * 3, rng.normal(size=64)
+    for act in (ops.ACT_GELU_TANH, ops.ACT_GELU_ERF, ops.ACT_SILU):
+        assert np.array_equal(ops.gated_activation(g, np.ones(64), act), ops.activation(g, act))
+        assert not ops.gated_activation(g, np.zeros(64), act).any()
+        assert np.allclose(ops.gated_activation(np.full(3, 50.0), u[:3], act), 50.0 * u[:3], rtol=1e-12)
+    assert np.allclose(ops.gelu_tanh(g), ops.gelu_erf(g), rtol=0, atol=1e-3)
+
+
 def test_rope_worked_example():
     g = load("rope_worked.json")
     u = np.array(g["u"]).reshape(1, 1, 4)
