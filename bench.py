@@ -12,6 +12,7 @@ own seeded synthetic inputs already resident in HBM:
   qwen3_qkv            packed QKV [4096, 48*128], per-head norm, 1D RoPE; four calls on
                        four buffer sets (100 MB each, under the L2 size) back to back
   chameleon_qkv_ln     packed QKV [4096, 96*128], per-head LayerNorm (weight + bias), 1D RoPE
+  swiglu_ffn           silu(gate) * up over [gate | up] bf16 [4096, 2*11008]
   wan_qkv3d            packed QKV [32760, 3*5120], full-width norm, 3D RoPE
   linear_bias_gelu     X [8192, 4096] . W[16384, 4096]^T + b, GELU(tanh)
   bn_fold              W [16384, 4096], BN of its 16384 output channels
@@ -284,6 +285,33 @@ class QkvOp(Op):
         return [st[0] for st in self.sets] + params, [t for st in self.sets for t in st[1:]]
 
 
+class GatedActOp(Op):
+    """SwiGLU: y = silu(gate) * up over [gate | up] rows."""
+
+    def __init__(self, gbf, name, case, act):
+        import torch
+        from workloads import as_torch as from_bits
+        self.gbf, self.name, self.act = gbf, name, act
+        self.rows, self.d = case["rows"], case["d"]
+        self.x = from_bits(case["x"])
+        self.y = torch.empty(self.rows, self.d, dtype=torch.bfloat16, device="cuda")
+
+    def run(self):
+        self.gbf.gated_act(self.x, self.y, self.act)
+
+    def algorithmic_bytes(self):
+        return self.rows * self.d * 6                  # read gate + up, write y (bf16)
+
+    def unfused_bytes(self):
+        return self.rows * self.d * 10                 # act: read g, write a; mul: read a, u, write y
+
+    def units(self):
+        return self.rows
+
+    def e2e_buffers(self):
+        return [self.x], [self.y]
+
+
 class GemmOp(Op):
     bound = "tensor"
 
@@ -346,8 +374,7 @@ class FoldOp(Op):
 
 
 OP_NAMES = ("add_rmsnorm_fp8", "pi05_ada_chain", "sweep_weighted", "sweep_noweight", "sweep_ada", "qwen3_qkv",
-            "chameleon_qkv_ln",
-            "wan_qkv3d", "linear_bias_gelu", "bn_fold")
+            "chameleon_qkv_ln", "swiglu_ffn", "wan_qkv3d", "linear_bias_gelu", "bn_fold")
 
 
 def build_ops(gbf, with_gemm, only=None, small=False):
@@ -369,6 +396,9 @@ def build_ops(gbf, with_gemm, only=None, small=False):
         ops.append(QkvOp(gbf, "qwen3_qkv", workloads.config_qwen3_qkv(), sets=1 if small else 4))
     if "chameleon_qkv_ln" in want:
         ops.append(QkvOp(gbf, "chameleon_qkv_ln", workloads.config_chameleon_qkv(tokens=2048 if small else 4096)))
+    if "swiglu_ffn" in want:
+        ops.append(GatedActOp(gbf, "swiglu_ffn", workloads.config_swiglu_ffn(rows=1024 if small else 4096),
+                              gbf.ACT_SILU))
     if "wan_qkv3d" in want:
         ops.append(QkvOp(gbf, "wan_qkv3d", workloads.config_wan_qkv(tokens=4096 if small else None)))
     if want & {"linear_bias_gelu", "bn_fold"}:
@@ -511,7 +541,7 @@ def kernel_source_hash(source):
 KERNEL_FILE = {"add_rmsnorm_fp8": "add_rmsnorm_fp8.cu", "pi05_ada_chain": "add_rmsnorm_fp8.cu",
                "sweep_weighted": "add_rmsnorm_fp8.cu", "sweep_noweight": "add_rmsnorm_fp8.cu",
                "sweep_ada": "add_rmsnorm_fp8.cu", "qwen3_qkv": "qkv_norm_rope.cu", "wan_qkv3d": "qkv_norm_rope.cu",
-               "chameleon_qkv_ln": "qkv_norm_rope.cu",
+               "chameleon_qkv_ln": "qkv_norm_rope.cu", "swiglu_ffn": "gated_act.cu",
                "linear_bias_gelu": "gemm_tcgen05.cu", "bn_fold": "bn_fold.cu"}
 
 
@@ -564,6 +594,10 @@ def cpu_baseline_sample(scale=1):
     dt = timed(lambda: chains.qkv_split_norm_rope(c["qkv"], 32, 32, 128, chains.QKNORM_LAYERNORM, c["q_w"], c["k_w"],
                                                   c["eps"], 0, c["pos"], c["theta"], q_b=c["q_b"], k_b=c["k_b"]))
     res["chameleon_qkv_ln"] = (bytes_qkv_layernorm(tc, 32, 32, 128), dt)
+    ts = 16 * scale
+    c = workloads.config_swiglu_ffn(rows=ts)
+    dt = timed(lambda: chains.gated_act(c["x"], 11008, 3))
+    res["swiglu_ffn"] = (ts * 11008 * 6, dt)
     tw = 64 * scale
     c = workloads.config_wan_qkv(tokens=tw)
     dt = timed(lambda: chains.qkv_split_norm_rope(c["qkv"], 40, 40, 128, 1, c["q_w"], c["k_w"], c["eps"], 1,
@@ -597,7 +631,8 @@ def run_cpu_baseline(scale=32):
     return {"value": round(d["gbs"], 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": (f"float64 numpy oracle, one thread: [16,256] add+RMSNorm+FP8; {min(10 * scale, 180)} of the 180 "
                        f"chained [10,1024] AdaRMSNorm calls; {64 * scale} rows of each [65536,4096] sweep; "
-                       f"{256 * scale} Qwen3 tokens; {128 * scale} Chameleon tokens; {64 * scale} Wan tokens; "
+                       f"{256 * scale} Qwen3 tokens; {128 * scale} Chameleon tokens; {16 * scale} SwiGLU rows; "
+                       f"{64 * scale} Wan tokens; "
                        f"BN fold of {1024 * scale} channels; "
                        "GB/s = algorithmic bytes / oracle time over the memory-bound operators (a "
                        f"{16 * scale}-row sample of the GEMM is in per_op as GFLOP/s)"),

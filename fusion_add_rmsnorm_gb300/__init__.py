@@ -28,7 +28,7 @@ OK, EINVAL, EALIGN, EUNSUPPORTED, ELAUNCH, ETIMEOUT, EDEVICE = 0, -1, -2, -3, -4
 NORM_WEIGHT, NORM_NOWEIGHT, NORM_ADA = 0, 1, 2
 QKNORM_PER_HEAD, QKNORM_FULL_WIDTH = 0, 1
 ROPE_1D, ROPE_3D = 0, 1
-ACT_NONE, ACT_GELU_TANH = 0, 1
+ACT_NONE, ACT_GELU_TANH, ACT_GELU_ERF, ACT_SILU = 0, 1, 2, 3
 
 _p, _i64, _i32, _f = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
 
@@ -39,6 +39,7 @@ _SIGNATURES = {
     "gbf_qkv_split_layernorm_rope": [_p, _i64, _i32, _i32, _i32, _p, _p, _p, _p, _f, _p, _f, _p, _p, _p, _p, _i64,
                                      _p],
     "gbf_linear_bias_gelu": [_p, _p, _p, _p, _i64, _i64, _i64, _i32, _p],
+    "gbf_gated_act": [_p, _p, _i64, _i64, _i32, _p],
     "gbf_bn_fold": [_p, _p, _p, _p, _p, _p, _f, _i64, _i64, _p, _p, _p],
     "gbf_copy": [_p, _p, _i64, _p],
     "gbf_device_status": [_p],
@@ -123,6 +124,12 @@ def linear_bias_gelu(x, w, bias, y, act=ACT_GELU_TANH, stream=None):
     m, k = x.shape
     n = w.shape[0]
     return _check(_lib.gbf_linear_bias_gelu(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), m, n, k, act, _stream(stream)))
+
+
+def gated_act(x, y, act=ACT_SILU, stream=None):
+    """gbf_gated_act: y[rows, d] = act(x[:, :d]) * x[:, d:] for x [rows, 2d]."""
+    rows, d = y.shape[0], y.shape[-1]
+    return _check(_lib.gbf_gated_act(_ptr(x), _ptr(y), rows, d, act, _stream(stream)))
 
 
 def bn_fold(w, b, gamma, beta, mean, var, eps, w_out, b_out, stream=None):

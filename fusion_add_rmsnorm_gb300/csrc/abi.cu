@@ -263,13 +263,35 @@ GBF_API int gbf_qkv_split_layernorm_rope(const void* qkv, int64_t tokens, int n_
                    v_cache, slots, cache_rows, stream);
 }
 
+// --------------------------------------------------- gated activation
+
+GBF_API int gbf_gated_act(const void* x, void* y, int64_t rows, int64_t d, int act, void* stream) {
+  const char* fn = "gbf_gated_act";
+  if (rows < 0 || d <= 0) return fail(GBF_EINVAL, "%s: rows >= 0 and d > 0 are required", fn);
+  if (act != GBF_ACT_GELU_TANH && act != GBF_ACT_GELU_ERF && act != GBF_ACT_SILU)
+    return fail(GBF_EINVAL, "%s: act must be GELU_TANH, GELU_ERF or SILU (got %d)", fn, act);
+  if (d % 8 != 0) return fail(GBF_EALIGN, "%s: d (%lld) must be a multiple of 8", fn, (long long)d);
+  if (rows == 0) return ok();
+  if (!x || !y) return fail(GBF_EINVAL, "%s: x and y are required", fn);
+  if (!aligned16(x) || !aligned16(y)) return fail(GBF_EALIGN, "%s: x and y must be 16-byte aligned", fn);
+  if (overlap(x, rows * 2 * d * 2, y, rows * d * 2)) return fail(GBF_EINVAL, "%s: y overlaps x", fn);
+  gbf::GatedActArgs a = {};
+  a.x = x;
+  a.y = y;
+  a.rows = rows;
+  a.d = d;
+  a.act = act;
+  return launch_status(gbf::launch_gated_act(a, static_cast<cudaStream_t>(stream)), fn);
+}
+
 // ------------------------------------------------ Linear + bias + GELU GEMM
 
 GBF_API int gbf_linear_bias_gelu(const void* X, const void* W, const void* bias, void* Y, int64_t M, int64_t N,
                                  int64_t K, int act, void* stream) {
   const char* fn = "gbf_linear_bias_gelu";
   if (M < 0 || N <= 0 || K <= 0) return fail(GBF_EINVAL, "%s: M >= 0, N > 0, K > 0 required", fn);
-  if (act != GBF_ACT_NONE && act != GBF_ACT_GELU_TANH) return fail(GBF_EINVAL, "%s: unknown activation %d", fn, act);
+  if (act != GBF_ACT_NONE && act != GBF_ACT_GELU_TANH && act != GBF_ACT_GELU_ERF && act != GBF_ACT_SILU)
+    return fail(GBF_EINVAL, "%s: unknown activation %d", fn, act);
   if (K % 64 != 0 || N % 16 != 0)
     return fail(GBF_EUNSUPPORTED, "%s: needs K %% 64 == 0 and N %% 16 == 0 (K=%lld, N=%lld)", fn, (long long)K,
                 (long long)N);

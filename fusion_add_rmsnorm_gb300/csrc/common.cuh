@@ -136,6 +136,28 @@ GBF_DEVICE float segment_sum(float v, int width) {
   return v;
 }
 
+// ------------------------------------------------------------ activations
+
+// GELU, tanh form 0.5 a (1 + tanh(0.7978845608 (a + 0.044715 a^3))).
+GBF_DEVICE float act_gelu_tanh(float a) {
+  const float inner = 0.7978845608f * fmaf(0.044715f * a, a * a, a);
+  return 0.5f * a * (1.0f + tanhf(inner));
+}
+// GELU, exact form 0.5 a (1 + erf(a / sqrt 2)).
+GBF_DEVICE float act_gelu_erf(float a) { return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f)); }
+// SiLU a / (1 + exp(-a)); for very negative a the quotient is a signed zero.
+GBF_DEVICE float act_silu(float a) { return a / (1.0f + expf(-a)); }
+
+// kActNone / kActGeluTanh / kActGeluErf / kActSilu (the enum of kernels.h).
+GBF_DEVICE float apply_act(float a, int act) {
+  switch (act) {
+    case 1: return act_gelu_tanh(a);
+    case 2: return act_gelu_erf(a);
+    case 3: return act_silu(a);
+    default: return a;
+  }
+}
+
 // --------------------------------------------- programmatic dependent launch
 
 // Wait until the grids this launch depends on have completed and their

@@ -125,11 +125,6 @@ GBF_DEVICE uint64_t smem_desc_sw128(uint32_t addr) {
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
                             (static_cast<uint32_t>(BM >> 4) << 24);
 
-GBF_DEVICE float gelu_tanh(float a) {
-  const float inner = 0.7978845608f * fmaf(0.044715f * a, a * a, a);
-  return 0.5f * a * (1.0f + tanhf(inner));
-}
-
 constexpr int kGroupN = 16;
 
 struct GemmParams {
@@ -296,7 +291,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float a = __uint_as_float(r[g * 8 + e]) + bz[e];
-            v[e] = p.act == kActGeluTanh ? gelu_tanh(a) : a;
+            v[e] = apply_act(a, p.act);
           }
           if (row < p.m) st_16(yrow + col, f32x8_to_bf16x8(v));
         }

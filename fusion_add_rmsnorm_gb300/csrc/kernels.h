@@ -10,7 +10,7 @@ namespace gbf {
 enum { kNormWeight = 0, kNormNoWeight = 1, kNormAda = 2 };
 enum { kQkNormPerHead = 0, kQkNormFullWidth = 1, kQkNormLayerNorm = 2 };
 enum { kRope1D = 0, kRope3D = 1 };
-enum { kActNone = 0, kActGeluTanh = 1 };
+enum { kActNone = 0, kActGeluTanh = 1, kActGeluErf = 2, kActSilu = 3 };
 
 // ------------------------------------------------------- add + RMSNorm + FP8
 struct AddRmsNormArgs {
@@ -75,6 +75,16 @@ struct QkvArgs {
 };
 
 cudaError_t launch_qkv_split_norm_rope(const QkvArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------- gated activation act(g) * u
+struct GatedActArgs {
+  const void* x;          // bf16 [rows, 2d]: gate | up
+  void* y;                // bf16 [rows, d]
+  int64_t rows, d;
+  int act;
+};
+
+cudaError_t launch_gated_act(const GatedActArgs& a, cudaStream_t stream);
 // True when the register-only per-head 1D kernel handles (norm, rope, d).  Every
 // other case stages a token's packed row (bf16) and its Q and K (float32) in
 // shared memory, which bounds (6 n_q + 8 n_kv) * d by kQkvStagedMaxBytes.

@@ -52,7 +52,7 @@ typedef enum {
 typedef enum { GBF_NORM_WEIGHT = 0, GBF_NORM_NOWEIGHT = 1, GBF_NORM_ADA = 2 } gbf_norm_mode;
 typedef enum { GBF_QKNORM_PER_HEAD = 0, GBF_QKNORM_FULL_WIDTH = 1 } gbf_qknorm;
 typedef enum { GBF_ROPE_1D = 0, GBF_ROPE_3D = 1 } gbf_rope;
-typedef enum { GBF_ACT_NONE = 0, GBF_ACT_GELU_TANH = 1 } gbf_act;
+typedef enum { GBF_ACT_NONE = 0, GBF_ACT_GELU_TANH = 1, GBF_ACT_GELU_ERF = 2, GBF_ACT_SILU = 3 } gbf_act;
 
 /*
  * gbf_add_rmsnorm_fp8 -- residual add (optionally gated), RMSNorm / _noweight /
@@ -161,7 +161,8 @@ GBF_API int gbf_qkv_split_layernorm_rope(const void* qkv, int64_t tokens, int n_
  *
  * X: device bf16 [M, K]; W: device bf16 [N, K] (nn.Linear [out, in] layout);
  * bias: device bf16 [N] or NULL (zero); Y: device bf16 [M, N].
- * act: GBF_ACT_GELU_TANH or GBF_ACT_NONE.
+ * act: GBF_ACT_GELU_TANH, GBF_ACT_NONE, GBF_ACT_GELU_ERF (0.5 a (1 + erf(a /
+ * sqrt 2)), the exact GELU of RFC §3.6) or GBF_ACT_SILU (a / (1 + exp(-a))).
  * Requires K % 64 == 0, N % 16 == 0, M >= 1 and 16-byte aligned X, W, Y
  * (GBF_EUNSUPPORTED / GBF_EALIGN otherwise); Y may not overlap X, W or bias.
  * The kernel's pipeline waits are bounded: a wait that gives up sets the
@@ -169,6 +170,20 @@ GBF_API int gbf_qkv_split_layernorm_rope(const void* qkv, int64_t tokens, int n_
  */
 GBF_API int gbf_linear_bias_gelu(const void* X, const void* W, const void* bias, void* Y, int64_t M,
                                  int64_t N, int64_t K, int act, void* stream);
+
+/*
+ * gbf_gated_act -- y = act(gate) * up in one pass: RFC §2.4 / §3.6 (silu
+ * gating -> npu_swiglu, gelu(x) * gate -> npu_gelu_mul; two elementwise ops
+ * whose intermediate act(gate) never reaches HBM).
+ *
+ * x: device bf16 [rows, 2d], each row the gate projection (columns 0..d-1)
+ * then the up projection (columns d..2d-1); y: device bf16 [rows, d].
+ * act: GBF_ACT_SILU (SwiGLU), GBF_ACT_GELU_TANH or GBF_ACT_GELU_ERF (GELU x
+ * Mul), else GBF_EINVAL.  Float32 arithmetic, one bf16 rounding per output.
+ * Requires d % 8 == 0 and 16-byte aligned x, y (GBF_EALIGN); y may not
+ * overlap x (GBF_EINVAL).
+ */
+GBF_API int gbf_gated_act(const void* x, void* y, int64_t rows, int64_t d, int act, void* stream);
 
 /*
  * gbf_bn_fold -- fold an inference BatchNorm into the weights of the producing

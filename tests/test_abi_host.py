@@ -27,7 +27,7 @@ def gbf():
 
 def test_header_declares_the_entry_points():
     assert declared_symbols() == sorted(["gbf_add_rmsnorm_fp8", "gbf_qkv_split_norm_rope",
-                                         "gbf_qkv_split_layernorm_rope", "gbf_linear_bias_gelu",
+                                         "gbf_qkv_split_layernorm_rope", "gbf_linear_bias_gelu", "gbf_gated_act",
                                          "gbf_bn_fold", "gbf_copy", "gbf_device_status", "gbf_last_error",
                                          "gbf_version", "gbf_selftest_bounded_wait"])
 
@@ -131,15 +131,34 @@ def test_qkv_layernorm_validation(gbf):
                                      ctypes.c_float(1e4), A(4), A(5), A(6), None, 4, None) == gbf.EINVAL
 
 
+def test_gated_act_validation(gbf):
+    L = gbf.raw()
+    call = lambda x=A(0), y=A(1), rows=4, d=64, act=gbf.ACT_SILU: L.gbf_gated_act(x, y, rows, d, act, None)  # noqa
+    assert call(rows=0) == gbf.OK
+    for act in (gbf.ACT_SILU, gbf.ACT_GELU_TANH, gbf.ACT_GELU_ERF):
+        assert call(rows=0, act=act) == gbf.OK
+    assert call(act=gbf.ACT_NONE) == gbf.EINVAL
+    assert call(act=9) == gbf.EINVAL
+    assert call(d=60) == gbf.EALIGN
+    assert call(d=0) == gbf.EINVAL
+    assert call(rows=-1) == gbf.EINVAL
+    assert call(x=None) == gbf.EINVAL
+    assert call(y=ctypes.c_void_p(F + 8)) == gbf.EALIGN
+    assert call(y=ctypes.c_void_p(F + 256)) == gbf.EINVAL     # y overlaps x
+
+
 def test_linear_and_fold_and_copy_validation(gbf):
     L = gbf.raw()
     lin = lambda **k: L.gbf_linear_bias_gelu(*[k.get(n, d) for n, d in [          # noqa: E731
         ("x", A(0)), ("w", A(1)), ("b", A(2)), ("y", A(3)), ("m", 128), ("n", 256), ("k", 128), ("act", 1),
         ("s", None)]])
     assert lin(m=0) == gbf.OK
+    for act in (gbf.ACT_NONE, gbf.ACT_GELU_TANH, gbf.ACT_GELU_ERF, gbf.ACT_SILU):
+        assert lin(m=0, act=act) == gbf.OK
+    assert lin(m=0, act=7) == gbf.EINVAL
     assert lin(k=100) == gbf.EUNSUPPORTED
     assert lin(n=8) == gbf.EUNSUPPORTED
-    assert lin(act=3) == gbf.EINVAL
+    assert lin(act=5) == gbf.EINVAL
     assert lin(x=None) == gbf.EINVAL
     assert lin(y=ctypes.c_void_p(4 * F + 2)) == gbf.EALIGN
     assert lin(y=A(0)) == gbf.EINVAL

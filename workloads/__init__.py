@@ -150,6 +150,18 @@ def config_wan_qkv(seed=0, tokens=None):
     return qkv_case(t, 40, 40, 128, 1, 1, seed, theta=1e4, grid=WAN_GRID, sections=(44, 42, 42))
 
 
+def gated_act_case(rows, d, seed=0, std=2.0):
+    """Gated-activation input bf16 [rows, 2d] = [gate | up], both ~ N(0, std):
+    gate values reach the saturated ends of SiLU and GELU."""
+    return {"x": Draw(seed).bf16_normal((rows, 2 * d), std=std), "rows": rows, "d": d}
+
+
+def config_swiglu_ffn(seed=0, rows=4096):
+    """SwiGLU on a LLaMA-7B-shaped FFN (intermediate width 11008): [gate | up]
+    bf16 [4096, 2*11008] -> silu(gate) * up bf16 [4096, 11008]."""
+    return gated_act_case(rows, 11008, seed)
+
+
 def linear_gelu_case(m, n, k, seed=0, with_bias=True):
     """X ~ N(0,1) [M, K], W ~ N(0, 0.02) [N, K], bias ~ N(0, 0.1) [N]; then the
     BatchNorm of the Linear's output channels: gamma ~ U(0.5, 1.5),
