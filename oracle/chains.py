@@ -12,7 +12,7 @@ oracle/ops.py.
 import numpy as np
 
 from . import ops
-from .formats import bf16_decode, bf16_encode, bf16_round
+from .formats import bf16_decode, bf16_encode, bf16_round, e4m3_decode
 
 NORM_WEIGHT, NORM_NOWEIGHT, NORM_ADA = 0, 1, 2
 QKNORM_PER_HEAD, QKNORM_FULL_WIDTH, QKNORM_LAYERNORM = 0, 1, 2
@@ -132,6 +132,30 @@ def linear_bias_gelu(x, w, bias=None, act_gelu=True, act=None):
     elif act_gelu:
         a = ops.gelu_tanh(a)
     return bf16_encode(a)
+
+
+def linear_fp8_act(xq, x_scale, wq, w_scale, bias=None, act=None):
+    """Quantised MatMul + activation (RFC §2.1 / §3.4: npu_quant_matmul_gelu,
+    A8W8 with a tanh or erf GELU): E4M3 activation codes [M, K] with one
+    descale (the codes fused_add_rmsnorm_fp8 writes, code * x_scale), E4M3
+    weight codes [N, K] with one descale per output channel, optional bf16
+    bias [N], then the activation (ops.ACT_*, None for none).  Exact float64
+    dot of the decoded values; output rounded once to bf16."""
+    a = ops.linear_dequant(e4m3_decode(xq), x_scale, e4m3_decode(wq), w_scale,
+                           None if bias is None else bf16_decode(bias))
+    if act is not None:
+        a = ops.activation(a, act)
+    return bf16_encode(a)
+
+
+def fold_norm_weight_bf16(w, gamma, gemma_style=True):
+    """Pre-fold of a norm weight into the next Linear's columns in binary32:
+    g = 1 + gamma (or gamma), W' = W * g, each one IEEE binary32 operation,
+    then one bf16 rounding (FlashRT §3, the `_noweight` kernel's weight).
+    w: bf16 bits [N, K]; gamma: bf16 bits [K]; returns bf16 bits [N, K]."""
+    wf = bf16_decode(w).astype(np.float32)
+    gf = bf16_decode(gamma).astype(np.float32)
+    return bf16_encode(ops.fold_norm_weight(wf, gf, gemma_style, dtype=np.float32).astype(np.float64))
 
 
 def gated_act(x, d, act):

@@ -260,6 +260,28 @@ def gated_activation(gate, up, act):
     return activation(gate, act) * np.asarray(up, np.float64)
 
 
+def fold_norm_weight(w, gamma, gemma_style=True, dtype=np.float64):
+    """Fold a norm's per-column weight into the next Linear (FlashRT §3: the
+    `_noweight` RMSNorm leaves its weight, Gemma-style 1 + gamma, to the next
+    GEMM): W'[n, k] = W[n, k] * (1 + gamma[k]) (or * gamma[k]), since
+    Linear(y * g) = y @ (W * g)^T.  In `dtype` one operation per step: g, then
+    the product."""
+    w = np.asarray(w, dtype)
+    gamma = np.asarray(gamma, dtype)
+    g = (dtype(1.0) + gamma) if gemma_style else gamma
+    return w * g[None, :]
+
+
+def linear_dequant(xq, x_scale, wq, w_scale, b=None):
+    """Quantised Linear (RFC §2.1 / §3.4, npu_quant_matmul with x1Scale and
+    x2Scale): y = (xq * x_scale) @ (wq * w_scale[:, None])^T + b, with the
+    integer-valued or FP8 operands given as their real values, one per-tensor
+    activation scale and one scale per weight row (output channel)."""
+    x = np.asarray(xq, np.float64) * np.float64(x_scale)
+    w = np.asarray(wq, np.float64) * np.asarray(w_scale, np.float64)[:, None]
+    return linear(x, w, b)
+
+
 # -------------------------------------------------------------- BatchNorm
 
 

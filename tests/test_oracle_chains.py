@@ -166,6 +166,29 @@ def test_gated_act_splits_gate_then_up_and_rounds_once():
     assert np.array_equal(both[1:2], chains.gated_act(np.concatenate([gate, up], axis=1)[1:2], d, ops.ACT_SILU))
 
 
+def test_linear_fp8_act_decodes_codes_and_applies_scales():
+    """Codes decode through the E4M3 table: 0x38 = 1.0, 0x40 = 2.0, 0xB8 = -1.0,
+    0x00 = 0; a hand-summed 1 x 2 by 2 x 2 case, then the activation."""
+    xq = np.array([[0x38, 0x40]], np.uint8)                   # (1, 2)
+    wq = np.array([[0x38, 0xB8], [0x40, 0x00]], np.uint8)     # rows (1, -1), (2, 0)
+    y = chains.linear_fp8_act(xq, 0.5, wq, np.array([1.0, 0.25], np.float32))
+    # row 0: 0.5 * (1*1 + 2*(-1)) * 1.0 = -0.5; row 1: 0.5 * (1*2 + 0) * 0.25 = 0.25
+    assert bf16_decode(y).tolist() == [[-0.5, 0.25]]
+    b = bf16_encode(np.array([1.0, -1.0]))
+    y = chains.linear_fp8_act(xq, 0.5, wq, np.array([1.0, 0.25], np.float32), b, act=ops.ACT_SILU)
+    assert np.array_equal(y, bf16_encode(ops.silu(np.array([[0.5, -0.75]]))))
+
+
+def test_fold_norm_weight_bf16_rounds_once_in_binary32():
+    rng = np.random.default_rng(44)
+    w, g = _rand_bits(rng, (3, 16), 0, .05), _rand_bits(rng, 16, 0, .2)
+    out = chains.fold_norm_weight_bf16(w, g)
+    wf = bf16_decode(w).astype(np.float32)
+    gf = bf16_decode(g).astype(np.float32)
+    via_torch = (torch.from_numpy(wf) * (1.0 + torch.from_numpy(gf))).numpy()   # binary32 add, then multiply
+    assert np.array_equal(out, bf16_encode(via_torch.astype(np.float64)))
+
+
 def test_qkv_slots_permute_cache_rows():
     rng = np.random.default_rng(24)
     t, hq, hkv, d = 6, 2, 1, 8

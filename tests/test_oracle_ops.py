@@ -169,6 +169,40 @@ def test_gated_activation_is_gate_act_times_up():
     assert np.allclose(ops.gelu_tanh(g), ops.gelu_erf(g), rtol=0, atol=1e-3)
 
 
+def test_fold_norm_weight_equals_scaling_the_input_fp64():
+    """Linear(y * (1 + g)) with W equals Linear(y) with the folded W', and the
+    plain (non-Gemma) fold equals Linear(y * g)."""
+    rng = np.random.default_rng(12)
+    y, w, g = rng.normal(size=(5, 24)), rng.normal(size=(7, 24)), rng.normal(size=24) * 0.1
+    assert np.allclose(ops.linear(y * (1 + g), w), ops.linear(y, ops.fold_norm_weight(w, g)), rtol=1e-12, atol=1e-12)
+    assert np.allclose(ops.linear(y * g, w), ops.linear(y, ops.fold_norm_weight(w, g, gemma_style=False)),
+                       rtol=1e-12, atol=1e-12)
+
+
+def test_fold_norm_weight_worked_example():
+    """W = 1.5, gamma = 0.25: 1.5 * 1.25 = 1.875 exactly (binary32 too); a zero
+    Gemma weight leaves W unchanged."""
+    w = np.array([[1.5, -3.0]], np.float32)
+    out = ops.fold_norm_weight(w, np.array([0.25, 0.0], np.float32), dtype=np.float32)
+    assert out.dtype == np.float32 and out.tolist() == [[1.875, -3.0]]
+
+
+def test_linear_dequant_brute_force_and_scales():
+    """A 2 x 3 by 4 x 3 product written out term by term; doubling the
+    activation scale doubles the bias-free output; zero codes give the bias."""
+    xq = np.array([[1.0, -2.0, 0.5], [3.0, 0.0, -1.0]])
+    wq = np.array([[1.0, 1.0, 1.0], [0.5, -1.0, 2.0], [0.0, 4.0, -0.25], [1.5, 2.0, 3.0]])
+    sw = np.array([0.5, 2.0, 1.0, 0.25])
+    b = np.array([0.1, -0.2, 0.3, 0.0])
+    y = ops.linear_dequant(xq, 0.5, wq, sw, b)
+    for i in range(2):
+        for j in range(4):
+            want = b[j] + sum(xq[i, k] * 0.5 * wq[j, k] * sw[j] for k in range(3))
+            assert abs(y[i, j] - want) < 1e-15
+    assert np.allclose(ops.linear_dequant(xq, 1.0, wq, sw), 2 * ops.linear_dequant(xq, 0.5, wq, sw), rtol=0)
+    assert np.array_equal(ops.linear_dequant(np.zeros((2, 3)), 0.5, wq, sw, b), np.tile(b, (2, 1)))
+
+
 def test_rope_worked_example():
     g = load("rope_worked.json")
     u = np.array(g["u"]).reshape(1, 1, 4)
