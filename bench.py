@@ -15,7 +15,9 @@ own seeded synthetic inputs already resident in HBM:
   swiglu_ffn           silu(gate) * up over [gate | up] bf16 [4096, 2*11008]
   wan_qkv3d            packed QKV [32760, 3*5120], full-width norm, 3D RoPE
   linear_bias_gelu     X [8192, 4096] . W[16384, 4096]^T + b, GELU(tanh)
+  linear_fp8_gelu      E4M3 X [8192, 4096] . E4M3 W [16384, 4096]^T with descales + b, GELU(tanh)
   bn_fold              W [16384, 4096], BN of its 16384 output channels
+  fold_norm_weight     W [16384, 4096] * (1 + gamma[4096]) (the _noweight norm's weight pre-folded)
 
 Timing: every operator is bracketed by CUDA events on the stream it is
 launched on; L2 (129 MB) is flushed before each operator, outside the event
@@ -345,6 +347,76 @@ class GemmOp(Op):
         return [self.x, self.w, self.b], [self.y]
 
 
+class GemmFp8Op(Op):
+    """Quantised Linear + GELU(tanh): E4M3 activation codes [M, K] (descale
+    0.05) and weight codes [N, K] (per-row descales), bias, bf16 out.  The codes
+    are made on the device from the case's seeded values by torch's E4M3
+    conversion (input preparation, outside the timed region)."""
+    bound = "tensor"
+    peak_ratio = 2.0          # dense E4M3 vs bf16 on this part (nominal 4.5 / 2.25 PFLOP/s)
+
+    def __init__(self, gbf, case):
+        import torch
+        from workloads import as_torch as from_bits
+        self.gbf, self.name, self.c = gbf, "linear_fp8_gelu", case
+        x = torch.from_numpy(case["x"]).cuda()
+        w = torch.from_numpy(case["w"]).cuda()
+        self.ws = torch.from_numpy(case["w_scale"]).cuda()
+        self.xs = float(np.float32(case["x_scale"]))
+        self.xq = (x / self.xs).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        self.wq = (w / self.ws[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        del x, w
+        self.b = from_bits(case["bias"])
+        self.y = torch.empty(case["m"], case["n"], dtype=torch.bfloat16, device="cuda")
+
+    def run(self):
+        self.gbf.linear_fp8_act(self.xq, self.xs, self.wq, self.ws, self.b, self.y, self.gbf.ACT_GELU_TANH)
+
+    def flops(self):
+        c = self.c
+        return 2 * c["m"] * c["n"] * c["k"]
+
+    def algorithmic_bytes(self):
+        c = self.c
+        return c["m"] * c["k"] + c["n"] * c["k"] + 4 * c["n"] + 2 * c["n"] + 2 * c["m"] * c["n"]
+
+    def unfused_bytes(self):
+        y = self.c["m"] * self.c["n"] * 2
+        return self.algorithmic_bytes() + 2 * y + 2 * y          # + a separate dequant/bias and GELU pass
+
+    def units(self):
+        return self.c["m"]
+
+    def e2e_buffers(self):
+        return [self.xq, self.wq, self.ws, self.b], [self.y]
+
+
+class NormFoldOp(Op):
+    """Pre-fold of a Gemma-style norm weight (1 + gamma) into W [N, K]."""
+
+    def __init__(self, gbf, case):
+        import torch
+        from workloads import as_torch as from_bits
+        self.gbf, self.name, self.c = gbf, "fold_norm_weight", case
+        self.w, self.g = from_bits(case["w"]), from_bits(case["gamma"])
+        self.wo = torch.empty_like(self.w)
+
+    def run(self):
+        self.gbf.fold_norm_weight(self.w, self.g, self.wo)
+
+    def algorithmic_bytes(self):
+        return 2 * self.c["out_ch"] * self.c["inner"] * 2 + 2 * self.c["inner"]
+
+    def unfused_bytes(self):
+        return self.algorithmic_bytes()
+
+    def units(self):
+        return self.c["out_ch"]
+
+    def e2e_buffers(self):
+        return [self.w, self.g], [self.wo]
+
+
 class FoldOp(Op):
     def __init__(self, gbf, case):
         import torch
@@ -374,7 +446,8 @@ class FoldOp(Op):
 
 
 OP_NAMES = ("add_rmsnorm_fp8", "pi05_ada_chain", "sweep_weighted", "sweep_noweight", "sweep_ada", "qwen3_qkv",
-            "chameleon_qkv_ln", "swiglu_ffn", "wan_qkv3d", "linear_bias_gelu", "bn_fold")
+            "chameleon_qkv_ln", "swiglu_ffn", "wan_qkv3d", "linear_bias_gelu", "linear_fp8_gelu", "bn_fold",
+            "fold_norm_weight")
 
 
 def build_ops(gbf, with_gemm, only=None, small=False):
@@ -407,6 +480,10 @@ def build_ops(gbf, with_gemm, only=None, small=False):
             ops.append(GemmOp(gbf, lin))
         if "bn_fold" in want:
             ops.append(FoldOp(gbf, lin))
+    if with_gemm and "linear_fp8_gelu" in want:
+        ops.append(GemmFp8Op(gbf, workloads.fp8_linear_case(2048 if small else 8192, 16384, 4096)))
+    if "fold_norm_weight" in want:
+        ops.append(NormFoldOp(gbf, workloads.norm_fold_case(16384, 4096)))
     return ops
 
 
@@ -542,7 +619,8 @@ KERNEL_FILE = {"add_rmsnorm_fp8": "add_rmsnorm_fp8.cu", "pi05_ada_chain": "add_r
                "sweep_weighted": "add_rmsnorm_fp8.cu", "sweep_noweight": "add_rmsnorm_fp8.cu",
                "sweep_ada": "add_rmsnorm_fp8.cu", "qwen3_qkv": "qkv_norm_rope.cu", "wan_qkv3d": "qkv_norm_rope.cu",
                "chameleon_qkv_ln": "qkv_norm_rope.cu", "swiglu_ffn": "gated_act.cu",
-               "linear_bias_gelu": "gemm_tcgen05.cu", "bn_fold": "bn_fold.cu"}
+               "linear_bias_gelu": "gemm_tcgen05.cu", "bn_fold": "bn_fold.cu", "linear_fp8_gelu": "gemm_tcgen05.cu",
+               "fold_norm_weight": "bn_fold.cu"}
 
 
 # -------------------------------------------------------------- CPU baseline
@@ -607,16 +685,31 @@ def cpu_baseline_sample(scale=1):
     c = workloads.linear_gelu_case(mg, 16384, 4096, seed=0)
     dt = timed(lambda: chains.linear_bias_gelu(c["x"], c["w"], c["bias"]))
     res["linear_bias_gelu"] = (2 * mg * 16384 * 4096, dt)         # flops
+    mf = 16 * scale
+    c = workloads.fp8_linear_case(mf, 16384, 4096, seed=0)
+    import torch
+
+    def e4m3(v):   # input codes (outside the timed call): clamp, then torch's nearest-even conversion
+        return torch.from_numpy(np.ascontiguousarray(v, np.float32)).clamp(-448, 448).to(
+            torch.float8_e4m3fn).view(torch.uint8).numpy()
+    xq = e4m3(c["x"] / np.float32(c["x_scale"]))
+    wq = e4m3(c["w"] / c["w_scale"][:, None])
+    dt = timed(lambda: chains.linear_fp8_act(xq, np.float32(c["x_scale"]), wq, c["w_scale"], c["bias"], act=1))
+    res["linear_fp8_gelu"] = (2 * mf * 16384 * 4096, dt)       # flops
+    cf = 1024 * scale
+    c = workloads.norm_fold_case(cf, 4096)
+    dt = timed(lambda: chains.fold_norm_weight_bf16(c["w"], c["gamma"]))
+    res["fold_norm_weight"] = (2 * cf * 4096 * 2 + 2 * 4096, dt)
     ch = 1024 * scale
     c = workloads.linear_gelu_case(1, ch, 4096, seed=0)
     dt = timed(lambda: chains.bn_fold_bf16(c["w"], c["bias"], c["gamma"], c["beta"], c["mean"], c["var"], c["eps"]))
     res["bn_fold"] = (2 * ch * 4096 * 2 + 2 * ch * 2 + 4 * ch * 4, dt)
     for k, (b, dt) in res.items():
-        if k != "linear_bias_gelu":
+        if k not in ("linear_bias_gelu", "linear_fp8_gelu"):
             t_total += dt
             byts_total += b
     return {"gbs": byts_total / t_total / 1e9, "seconds": t_total,
-            "per_op": {k: ({"gflops": b / dt / 1e9} if k == "linear_bias_gelu" else {"gbs": b / dt / 1e9})
+            "per_op": {k: ({"gflops": b / dt / 1e9} if k in ("linear_bias_gelu", "linear_fp8_gelu") else {"gbs": b / dt / 1e9})
                        for k, (b, dt) in res.items()}}
 
 
@@ -633,9 +726,9 @@ def run_cpu_baseline(scale=32):
                        f"chained [10,1024] AdaRMSNorm calls; {64 * scale} rows of each [65536,4096] sweep; "
                        f"{256 * scale} Qwen3 tokens; {128 * scale} Chameleon tokens; {16 * scale} SwiGLU rows; "
                        f"{64 * scale} Wan tokens; "
-                       f"BN fold of {1024 * scale} channels; "
+                       f"BN fold and norm-weight fold of {1024 * scale} channels each; "
                        "GB/s = algorithmic bytes / oracle time over the memory-bound operators (a "
-                       f"{16 * scale}-row sample of the GEMM is in per_op as GFLOP/s)"),
+                       f"{16 * scale}-row sample of each GEMM is in per_op as GFLOP/s)"),
             "seconds": round(d["seconds"], 3), "per_op": d["per_op"]}
 
 
@@ -738,7 +831,8 @@ def main_gpu(args):
         entry = {"ms": round(ms, 5), "launches": op.launches, "tokens_per_s": round(op.units() / (ms / 1e3), 1)}
         if op.bound == "tensor":
             tf = op.flops() / (ms / 1e3) / 1e12
-            entry.update({"tflops": round(tf, 1), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+            peak = peaks["bf16_tflops"] * getattr(op, "peak_ratio", 1.0)
+            entry.update({"tflops": round(tf, 1), "frac_of_peak": round(tf / peak, 4), "peak_tflops": round(peak, 1),
                           "bytes": op.algorithmic_bytes()})
         else:
             gbs = op.algorithmic_bytes() / (ms / 1e3) / 1e9

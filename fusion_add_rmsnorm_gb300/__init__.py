@@ -40,6 +40,8 @@ _SIGNATURES = {
                                      _p],
     "gbf_linear_bias_gelu": [_p, _p, _p, _p, _i64, _i64, _i64, _i32, _p],
     "gbf_gated_act": [_p, _p, _i64, _i64, _i32, _p],
+    "gbf_linear_fp8_act": [_p, _f, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p],
+    "gbf_fold_norm_weight": [_p, _p, _i32, _i64, _i64, _p, _p],
     "gbf_bn_fold": [_p, _p, _p, _p, _p, _p, _f, _i64, _i64, _p, _p, _p],
     "gbf_copy": [_p, _p, _i64, _p],
     "gbf_device_status": [_p],
@@ -124,6 +126,22 @@ def linear_bias_gelu(x, w, bias, y, act=ACT_GELU_TANH, stream=None):
     m, k = x.shape
     n = w.shape[0]
     return _check(_lib.gbf_linear_bias_gelu(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), m, n, k, act, _stream(stream)))
+
+
+def linear_fp8_act(xq, x_scale, wq, w_scale, bias, y, act=ACT_GELU_TANH, stream=None):
+    """gbf_linear_fp8_act: y[M, N] = act((xq * x_scale) @ (wq * w_scale[:, None])^T + bias); xq, wq uint8 codes."""
+    m, k = xq.shape
+    n = wq.shape[0]
+    return _check(_lib.gbf_linear_fp8_act(_ptr(xq), x_scale, _ptr(wq), _ptr(w_scale), _ptr(bias), _ptr(y), m, n, k,
+                                          act, _stream(stream)))
+
+
+def fold_norm_weight(w, gamma, w_out, gemma_style=True, stream=None):
+    """gbf_fold_norm_weight: w_out = w * (1 + gamma) (or w * gamma), per column."""
+    out_ch = w.shape[0]
+    inner = w.numel() // max(out_ch, 1)
+    return _check(_lib.gbf_fold_norm_weight(_ptr(w), _ptr(gamma), 1 if gemma_style else 0, out_ch, inner,
+                                            _ptr(w_out), _stream(stream)))
 
 
 def gated_act(x, y, act=ACT_SILU, stream=None):

@@ -286,29 +286,40 @@ GBF_API int gbf_gated_act(const void* x, void* y, int64_t rows, int64_t d, int a
 
 // ------------------------------------------------ Linear + bias + GELU GEMM
 
-GBF_API int gbf_linear_bias_gelu(const void* X, const void* W, const void* bias, void* Y, int64_t M, int64_t N,
-                                 int64_t K, int act, void* stream) {
-  const char* fn = "gbf_linear_bias_gelu";
+namespace {
+
+// Both Linear entry points: bf16 operands, or E4M3 codes with descales.
+int linear_entry(const char* fn, bool fp8, const void* X, float x_scale, const void* W, const float* w_scale,
+                 const void* bias, void* Y, int64_t M, int64_t N, int64_t K, int act, void* stream) {
   if (M < 0 || N <= 0 || K <= 0) return fail(GBF_EINVAL, "%s: M >= 0, N > 0, K > 0 required", fn);
   if (act != GBF_ACT_NONE && act != GBF_ACT_GELU_TANH && act != GBF_ACT_GELU_ERF && act != GBF_ACT_SILU)
     return fail(GBF_EINVAL, "%s: unknown activation %d", fn, act);
-  if (K % 64 != 0 || N % 16 != 0)
-    return fail(GBF_EUNSUPPORTED, "%s: needs K %% 64 == 0 and N %% 16 == 0 (K=%lld, N=%lld)", fn, (long long)K,
-                (long long)N);
+  if (fp8 && (!(x_scale > 0.0f) || !std::isfinite(x_scale)))
+    return fail(GBF_EINVAL, "%s: x_scale must be finite and > 0", fn);
+  const int64_t kq = fp8 ? 128 : 64;
+  if (K % kq != 0 || N % 16 != 0)
+    return fail(GBF_EUNSUPPORTED, "%s: needs K %% %lld == 0 and N %% 16 == 0 (K=%lld, N=%lld)", fn, (long long)kq,
+                (long long)K, (long long)N);
   if (M > (1LL << 31) || N > (1LL << 31) || K > (1LL << 31))
     return fail(GBF_EUNSUPPORTED, "%s: extents must be below 2^31", fn);
   if (M == 0) return ok();
-  if (!X || !W || !Y) return fail(GBF_EINVAL, "%s: X, W, Y are required", fn);
-  if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || (bias && !aligned16(bias)))
-    return fail(GBF_EALIGN, "%s: X, W, Y, bias must be 16-byte aligned", fn);
+  if (!X || !W || !Y || (fp8 && !w_scale)) return fail(GBF_EINVAL, "%s: X, W, Y (and w_scale) are required", fn);
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || (bias && !aligned16(bias)) ||
+      (w_scale && !aligned16(w_scale)))
+    return fail(GBF_EALIGN, "%s: X, W, Y, bias, w_scale must be 16-byte aligned", fn);
+  const int64_t es = fp8 ? 1 : 2;
   const int64_t yb = M * N * 2;
-  if (overlap(Y, yb, X, M * K * 2) || overlap(Y, yb, W, N * K * 2) || overlap(Y, yb, bias, N * 2))
+  if (overlap(Y, yb, X, M * K * es) || overlap(Y, yb, W, N * K * es) || overlap(Y, yb, bias, N * 2) ||
+      overlap(Y, yb, w_scale, fp8 ? N * 4 : 0))
     return fail(GBF_EINVAL, "%s: Y overlaps an input", fn);
   gbf::GemmArgs a = {};
   a.x = X;
   a.w = W;
   a.bias = bias;
   a.y = Y;
+  a.w_scale = w_scale;
+  a.x_scale = x_scale;
+  a.fp8 = fp8 ? 1 : 0;
   a.err = error_word();
   a.m = M;
   a.n = N;
@@ -318,6 +329,40 @@ GBF_API int gbf_linear_bias_gelu(const void* X, const void* W, const void* bias,
   cudaError_t e = gbf::launch_linear_bias_gelu(a, static_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess && why) return fail(GBF_ELAUNCH, "%s: %s (%s)", fn, why, cudaGetErrorString(e));
   return launch_status(e, fn);
+}
+
+}  // namespace
+
+GBF_API int gbf_linear_bias_gelu(const void* X, const void* W, const void* bias, void* Y, int64_t M, int64_t N,
+                                 int64_t K, int act, void* stream) {
+  return linear_entry("gbf_linear_bias_gelu", false, X, 1.0f, W, nullptr, bias, Y, M, N, K, act, stream);
+}
+
+GBF_API int gbf_linear_fp8_act(const uint8_t* Xq, float x_scale, const uint8_t* Wq, const float* w_scale,
+                               const void* bias, void* Y, int64_t M, int64_t N, int64_t K, int act, void* stream) {
+  return linear_entry("gbf_linear_fp8_act", true, Xq, x_scale, Wq, w_scale, bias, Y, M, N, K, act, stream);
+}
+
+// ------------------------------------------------ norm weight pre-fold
+
+GBF_API int gbf_fold_norm_weight(const void* W, const void* gamma, int gemma_style, int64_t out_ch, int64_t inner,
+                                 void* W_out, void* stream) {
+  const char* fn = "gbf_fold_norm_weight";
+  if (out_ch < 0 || inner <= 0) return fail(GBF_EINVAL, "%s: out_ch >= 0 and inner > 0 required", fn);
+  if (gemma_style != 0 && gemma_style != 1) return fail(GBF_EINVAL, "%s: gemma_style must be 0 or 1", fn);
+  if (out_ch == 0) return ok();
+  if (!W || !gamma || !W_out) return fail(GBF_EINVAL, "%s: W, gamma and W_out are required", fn);
+  const int64_t wb = out_ch * inner * 2;
+  if (W_out != W && overlap(W_out, wb, W, wb)) return fail(GBF_EINVAL, "%s: W_out partially overlaps W", fn);
+  if (overlap(W_out, wb, gamma, inner * 2)) return fail(GBF_EINVAL, "%s: W_out overlaps gamma", fn);
+  gbf::NormFoldArgs a = {};
+  a.w = W;
+  a.gamma = gamma;
+  a.w_out = W_out;
+  a.out_ch = out_ch;
+  a.inner = inner;
+  a.gemma = gemma_style;
+  return launch_status(gbf::launch_fold_norm_weight(a, static_cast<cudaStream_t>(stream)), fn);
 }
 
 // ------------------------------------------------------------ BN folding

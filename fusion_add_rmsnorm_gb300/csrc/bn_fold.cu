@@ -74,7 +74,66 @@ __global__ void __launch_bounds__(kBnBlock) bn_fold_kernel(const BnFoldArgs a) {
   }
 }
 
+// Norm-weight pre-fold (FlashRT §3, the `_noweight` RMSNorm's Gemma-style
+// weight moved into the next GEMM): W'[c, k] = W[c, k] * g[k] with
+// g = 1 + gamma (gemma) or gamma, each one binary32 operation, then one bf16
+// rounding.  Same layout as the BN fold: a warp per output row.
+template <bool VEC>
+__global__ void __launch_bounds__(kBnBlock) fold_norm_weight_kernel(const NormFoldArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kBnBlock + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kBnBlock) >> 5;
+  const __nv_bfloat16* gam = static_cast<const __nv_bfloat16*>(a.gamma);
+  auto g_of = [&](float gv) { return a.gemma ? __fadd_rn(1.0f, gv) : gv; };
+  for (int64_t c = warp; c < a.out_ch; c += nwarps) {
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.w) + c * a.inner;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.w_out) + c * a.inner;
+    if (VEC) {
+      const int nvec = static_cast<int>(a.inner >> 3);
+      for (int base = 0; base < nvec; base += 32 * kBnUnroll) {
+        uint4 v[kBnUnroll];
+#pragma unroll
+        for (int k = 0; k < kBnUnroll; ++k) {
+          const int i = base + k * 32 + lane;
+          if (i < nvec) v[k] = ld_stream(src + i * 8);
+        }
+#pragma unroll
+        for (int k = 0; k < kBnUnroll; ++k) {
+          const int i = base + k * 32 + lane;
+          if (i < nvec) {
+            float f[8], gv[8];
+            bf16x8_to_f32(v[k], f);
+            bf16x8_to_f32(ld_cached(gam + i * 8), gv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(f[e], g_of(gv[e]));
+            st_16(dst + i * 8, f32x8_to_bf16x8(f));
+          }
+        }
+      }
+    } else {
+      for (int64_t i = lane; i < a.inner; i += 32)
+        dst[i] = __float2bfloat16_rn(__fmul_rn(__bfloat162float(src[i]), g_of(__bfloat162float(gam[i]))));
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_fold_norm_weight(const NormFoldArgs& a, cudaStream_t stream) {
+  if (a.out_ch == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (a.out_ch + (kBnBlock / 32) - 1) / (kBnBlock / 32);
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * 8;
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  const bool vec = (a.inner % 8 == 0) && (reinterpret_cast<uintptr_t>(a.w) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(a.w_out) % 16 == 0) && (reinterpret_cast<uintptr_t>(a.gamma) % 16 == 0);
+  return vec ? launch_pdl(fold_norm_weight_kernel<true>, dim3(grid), dim3(kBnBlock), 0, stream, a)
+             : launch_pdl(fold_norm_weight_kernel<false>, dim3(grid), dim3(kBnBlock), 0, stream, a);
+}
 
 cudaError_t launch_bn_fold(const BnFoldArgs& a, cudaStream_t stream) {
   if (a.out_ch == 0) return cudaSuccess;

@@ -44,11 +44,11 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int UMMA_K = 16;
+constexpr int BK_BYTES = 128;                    // one 128-byte swizzle row of K per k-block
+constexpr int UMMA_K_BYTES = 32;                 // K of one MMA: 16 bf16 or 32 E4M3 values
 constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;       // 16 KB
-constexpr int B_STAGE_BYTES = BN * BK * 2;       // 32 KB
+constexpr int A_STAGE_BYTES = BM * BK_BYTES;     // 16 KB
+constexpr int B_STAGE_BYTES = BN * BK_BYTES;     // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;                // two accumulators
 constexpr int kThreads = 256;
@@ -83,14 +83,25 @@ GBF_DEVICE void tc_commit(uint64_t* bar) {
                : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, float32 accumulator).
+// D[tmem] (+)= A[smem] * B[smem]^T with a float32 accumulator: kind::f16 for
+// bf16 operands, kind::f8f6f4 for E4M3 operands (both operands one type).
+template <bool FP8>
 GBF_DEVICE void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if (FP8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 
 // 32 consecutive float32 columns of this warp's 32 TMEM lanes, one lane per thread.
@@ -120,16 +131,20 @@ GBF_DEVICE uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: float32 D, bf16 A and B, both K-major,
-// N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
+// Instruction descriptors: float32 D (bits 4-5 = 1), A and B type codes at
+// bits 7-9 and 10-12 (kind::f16: bf16 = 1; kind::f8f6f4: E4M3 = 0), both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t kIdescShape = (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | kIdescShape;
+constexpr uint32_t kIdescE4m3 = (1u << 4) | (0u << 7) | (0u << 10) | kIdescShape;
 
 constexpr int kGroupN = 16;
 
 struct GemmParams {
   const __nv_bfloat16* bias;
   __nv_bfloat16* y;
+  const float* w_scale;      // E4M3 weights: descale per output channel
+  float x_scale;             // E4M3 activations: the descale
   unsigned int* err;
   int m, n, k;
   int m_tiles, n_tiles;
@@ -147,9 +162,12 @@ GBF_DEVICE void tile_origin(const GemmParams& p, int tile, int& m0, int& n0) {
   n0 = (n_base + idx % gs) * BN;
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                         const GemmParams p) {
+  constexpr int BK = FP8 ? BK_BYTES : BK_BYTES / 2;         // K elements per k-block
+  constexpr uint32_t kIdesc = FP8 ? kIdescE4m3 : kIdescBf16;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smem_a = smem;                                   // STAGES x 16 KB
@@ -240,11 +258,11 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
           const uint32_t a_addr = smem_u32(smem_a + stage * A_STAGE_BYTES);
           const uint32_t b_addr = smem_u32(smem_b + stage * B_STAGE_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            // advance 16 elements (32 bytes) along K inside the swizzled row
-            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * UMMA_K * 2);
-            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * UMMA_K * 2);
-            tc_mma(d_tmem, a_desc, b_desc, kIdesc, (kb | kk) != 0);
+          for (int kk = 0; kk < BK_BYTES / UMMA_K_BYTES; ++kk) {
+            // advance one MMA's K (32 bytes) inside the swizzled row
+            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * UMMA_K_BYTES);
+            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * UMMA_K_BYTES);
+            tc_mma<FP8>(d_tmem, a_desc, b_desc, kIdesc, (kb | kk) != 0);
           }
           tc_commit(&ctl->empty[stage]);      // frees the stage once these MMAs have read it
           if (++stage == STAGES) {
@@ -288,9 +306,18 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
           float v[8];
           float bz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
           if (p.bias) bf16x8_to_f32(ld_cached(p.bias + col), bz);
+          float sc[8];
+          if (FP8) {                                      // descales: activation x weight row
+            const float4 s0 = *reinterpret_cast<const float4*>(p.w_scale + col);
+            const float4 s1 = *reinterpret_cast<const float4*>(p.w_scale + col + 4);
+            const float ws[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sc[e] = p.x_scale * ws[e];
+          }
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float a = __uint_as_float(r[g * 8 + e]) + bz[e];
+            const float acc = __uint_as_float(r[g * 8 + e]);
+            const float a = FP8 ? fmaf(acc, sc[e], bz[e]) : acc + bz[e];
             v[e] = apply_act(a, p.act);
           }
           if (row < p.m) st_16(yrow + col, f32x8_to_bf16x8(v));
@@ -332,15 +359,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2D bf16 tensor [rows, cols] (cols contiguous), box [box_rows, 64], 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+// 2D tensor [rows, cols] (cols contiguous) of bf16 or of bytes (E4M3), box
+// [box_rows, 128 bytes of K], 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, bool fp8) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const int esize = fp8 ? 1 : 2;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * esize};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK_BYTES / esize), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+            dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -349,13 +379,16 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
 
 cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, const char** why) {
   CUtensorMap map_x, map_w;
-  if (!make_map(&map_x, a.x, a.m, a.k, BM) || !make_map(&map_w, a.w, a.n, a.k, BN)) {
+  const bool fp8 = a.fp8 != 0;
+  if (!make_map(&map_x, a.x, a.m, a.k, BM, fp8) || !make_map(&map_w, a.w, a.n, a.k, BN, fp8)) {
     *why = "cuTensorMapEncodeTiled is unavailable or rejected the operands";
     return cudaErrorInvalidValue;
   }
   GemmParams p;
   p.bias = static_cast<const __nv_bfloat16*>(a.bias);
   p.y = static_cast<__nv_bfloat16*>(a.y);
+  p.w_scale = a.w_scale;
+  p.x_scale = a.x_scale;
   p.err = a.err;
   p.m = static_cast<int>(a.m);
   p.n = static_cast<int>(a.n);
@@ -368,13 +401,13 @@ cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, cons
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < sms ? tiles : sms;
-  cudaError_t e = cudaFuncSetAttribute(linear_bias_gelu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+  auto kern = fp8 ? linear_bias_gelu_kernel<true> : linear_bias_gelu_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) {
     *why = "could not reserve shared memory";
     return e;
   }
-  linear_bias_gelu_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_x, map_w, p);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(map_x, map_w, p);
   return cudaGetLastError();
 }
 

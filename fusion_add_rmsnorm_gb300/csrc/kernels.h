@@ -116,14 +116,28 @@ cudaError_t launch_bounded_wait_selftest(unsigned int* err, cudaStream_t stream)
 
 // ------------------------------------------------ Linear + bias + GELU GEMM
 struct GemmArgs {
-  const void* x;          // [M, K] bf16, K-major
-  const void* w;          // [N, K] bf16, K-major
+  const void* x;          // [M, K] bf16 (or E4M3 codes when fp8), K-major
+  const void* w;          // [N, K] bf16 (or E4M3 codes when fp8), K-major
   const void* bias;       // [N] bf16, nullable
   void* y;                // [M, N] bf16
+  const float* w_scale;   // fp8: [N] weight descales
+  float x_scale;          // fp8: activation descale
+  int fp8;
   unsigned int* err;
   int64_t m, n, k;
   int act;
 };
+
+// ------------------------------------------------------- weight folding
+struct NormFoldArgs {
+  const void* w;          // [out_ch, inner] bf16
+  const void* gamma;      // [inner] bf16
+  void* w_out;            // [out_ch, inner] bf16 (may equal w)
+  int64_t out_ch, inner;
+  int gemma;              // W * (1 + gamma) when set, else W * gamma
+};
+
+cudaError_t launch_fold_norm_weight(const NormFoldArgs& a, cudaStream_t stream);
 
 cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, const char** why);
 

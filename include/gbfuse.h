@@ -186,6 +186,40 @@ GBF_API int gbf_linear_bias_gelu(const void* X, const void* W, const void* bias,
 GBF_API int gbf_gated_act(const void* x, void* y, int64_t rows, int64_t d, int act, void* stream);
 
 /*
+ * gbf_linear_fp8_act -- Y = act((Xq * x_scale) (Wq * w_scale)^T + bias): the
+ * quantised MatMul + activation of RFC §2.1 / §3.4 (npu_quant_matmul_gelu
+ * with its activation and weight scales), on the tcgen05 tensor cores
+ * (kind::f8f6f4, E4M3 x E4M3, float32 accumulation in tensor memory); the
+ * descales, bias and activation are applied to the accumulator tile before
+ * the single bf16 store.  Xq are E4M3 codes such as gbf_add_rmsnorm_fp8
+ * writes (code * x_scale is the value).
+ *
+ * Xq: device uint8 E4M3 codes [M, K]; x_scale: the activations' descale
+ * (finite, > 0); Wq: device uint8 E4M3 codes [N, K] (nn.Linear [out, in]
+ * layout); w_scale: device float32 [N], the descale of each weight row; bias:
+ * device bf16 [N] or NULL; Y: device bf16 [M, N]; act as gbf_linear_bias_gelu.
+ * Requires K % 128 == 0, N % 16 == 0 and 16-byte aligned Xq, Wq, w_scale, Y
+ * (GBF_EUNSUPPORTED / GBF_EALIGN); Y may not overlap an input.  Waits are
+ * bounded as in gbf_linear_bias_gelu.
+ */
+GBF_API int gbf_linear_fp8_act(const uint8_t* Xq, float x_scale, const uint8_t* Wq, const float* w_scale,
+                               const void* bias, void* Y, int64_t M, int64_t N, int64_t K, int act, void* stream);
+
+/*
+ * gbf_fold_norm_weight -- move a norm's per-column weight into the next
+ * Linear: W_out[c, k] = W[c, k] * (1 + gamma[k]) (gemma_style = 1, the
+ * Gemma-style weight that FlashRT §3's `_noweight` RMSNorm leaves to the
+ * next GEMM) or W[c, k] * gamma[k] (gemma_style = 0).  Binary32, one IEEE
+ * operation per step (the sum, then the product), then one bf16 rounding:
+ * bit-reproducible.
+ *
+ * W: device bf16 [out_ch, inner]; gamma: device bf16 [inner]; W_out: device
+ * bf16 [out_ch, inner], may equal W (in place); other overlaps GBF_EINVAL.
+ */
+GBF_API int gbf_fold_norm_weight(const void* W, const void* gamma, int gemma_style, int64_t out_ch, int64_t inner,
+                                 void* W_out, void* stream);
+
+/*
  * gbf_bn_fold -- fold an inference BatchNorm into the weights of the producing
  * Conv or Linear.  OpenPPL §3.1 (scale = gamma / sqrt(var + eps);
  * W' = W * scale per output channel; b' = (b - mean) * scale + beta; missing

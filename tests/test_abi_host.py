@@ -28,6 +28,7 @@ def gbf():
 def test_header_declares_the_entry_points():
     assert declared_symbols() == sorted(["gbf_add_rmsnorm_fp8", "gbf_qkv_split_norm_rope",
                                          "gbf_qkv_split_layernorm_rope", "gbf_linear_bias_gelu", "gbf_gated_act",
+                                         "gbf_linear_fp8_act", "gbf_fold_norm_weight",
                                          "gbf_bn_fold", "gbf_copy", "gbf_device_status", "gbf_last_error",
                                          "gbf_version", "gbf_selftest_bounded_wait"])
 
@@ -145,6 +146,30 @@ def test_gated_act_validation(gbf):
     assert call(x=None) == gbf.EINVAL
     assert call(y=ctypes.c_void_p(F + 8)) == gbf.EALIGN
     assert call(y=ctypes.c_void_p(F + 256)) == gbf.EINVAL     # y overlaps x
+
+
+def test_linear_fp8_and_norm_fold_validation(gbf):
+    L = gbf.raw()
+    lin = lambda **k: L.gbf_linear_fp8_act(*[k.get(n, d) for n, d in [              # noqa: E731
+        ("x", A(0)), ("xs", 0.05), ("w", A(1)), ("ws", A(2)), ("b", A(3)), ("y", A(4)), ("m", 128), ("n", 256),
+        ("k", 256), ("act", 1), ("s", None)]])
+    assert lin(m=0) == gbf.OK
+    assert lin(k=192) == gbf.EUNSUPPORTED                    # K % 128
+    assert lin(n=8) == gbf.EUNSUPPORTED
+    assert lin(xs=0.0) == gbf.EINVAL
+    assert lin(xs=float("nan")) == gbf.EINVAL
+    assert lin(ws=None) == gbf.EINVAL
+    assert lin(act=6) == gbf.EINVAL
+    assert lin(ws=ctypes.c_void_p(2 * F + 4)) == gbf.EALIGN
+    assert lin(y=A(2)) == gbf.EINVAL                         # Y overlaps w_scale
+    fold = lambda **k: L.gbf_fold_norm_weight(*[k.get(n, d) for n, d in [          # noqa: E731
+        ("w", A(0)), ("g", A(1)), ("gemma", 1), ("oc", 8), ("inner", 64), ("wo", A(2)), ("s", None)]])
+    assert fold(oc=0) == gbf.OK
+    assert fold(inner=0) == gbf.EINVAL
+    assert fold(gemma=2) == gbf.EINVAL
+    assert fold(g=None) == gbf.EINVAL
+    assert fold(wo=ctypes.c_void_p(F + 16)) == gbf.EINVAL    # partial overlap with W
+    assert fold(wo=A(1)) == gbf.EINVAL                       # overlaps gamma
 
 
 def test_linear_and_fold_and_copy_validation(gbf):

@@ -189,3 +189,24 @@ def as_torch(bits, device="cuda"):
     if a.dtype == np.uint16:
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
     return torch.from_numpy(a).to(device)
+
+
+def fp8_linear_case(m, n, k, seed=0):
+    """Quantised Linear operands as real values before quantisation: X ~ N(0, 1)
+    [M, K] (the activations fused_add_rmsnorm_fp8 quantises, descale 0.05),
+    W ~ N(0, 0.02) [N, K], bias ~ N(0, 0.1) [N] (bf16 bits), and one weight
+    descale per row ~ U(0.9, 1.1) * 0.1 / 448 (about five standard deviations
+    of W at the top code).  The caller encodes the E4M3 codes (the oracle in
+    tests, a library conversion on the GPU in the bench)."""
+    d = Draw(seed)
+    return {"x": d.normal((m, k)), "w": d.normal((n, k), std=0.02), "bias": d.bf16_normal((n,), std=0.1),
+            "x_scale": 0.05, "w_scale": (d.uniform((n,), 0.9, 1.1) * (0.1 / 448.0)).astype(np.float32),
+            "m": m, "n": n, "k": k}
+
+
+def norm_fold_case(out_ch, inner, seed=0):
+    """W bf16 [out_ch, inner] ~ N(0, 0.02); a norm weight gamma bf16 [inner] ~
+    N(0, 0.1) (Gemma-style: the scale is 1 + gamma)."""
+    d = Draw(seed)
+    return {"w": d.bf16_normal((out_ch, inner), std=0.02), "gamma": d.bf16_normal((inner,), std=0.1),
+            "out_ch": out_ch, "inner": inner}
