@@ -148,6 +148,38 @@ GBF_DEVICE float act_gelu_erf(float a) { return 0.5f * a * (1.0f + erff(a * 0.70
 // SiLU a / (1 + exp(-a)); for very negative a the quotient is a signed zero.
 GBF_DEVICE float act_silu(float a) { return a / (1.0f + expf(-a)); }
 
+// Fast forms for epilogues, well inside one bf16 rounding:
+//  * tanh GELU with the hardware tanh approximation (tanh.approx.f32, relative
+//    error below 2^-10.9);
+//  * erf GELU with erf(x) = 1 - (a1 t + ... + a5 t^5) e^(-x^2), t = 1/(1 + p x)
+//    for x >= 0 (M. Abramowitz, I. Stegun, "Handbook of Mathematical
+//    Functions", 1964, formula 7.1.26; absolute error below 1.5e-7), odd in x;
+//  * SiLU with the fast exponential and division intrinsics.
+GBF_DEVICE float tanh_approx(float a) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(a));
+  return t;
+}
+GBF_DEVICE float erf_as7126(float x) {
+  const float ax = fabsf(x);
+  const float t = __frcp_rn(fmaf(0.3275911f, ax, 1.0f));
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  poly *= t;
+  const float y = 1.0f - poly * __expf(-ax * ax);
+  return copysignf(y, x);
+}
+GBF_DEVICE float fast_act(float a, int act) {
+  switch (act) {
+    case 1: return 0.5f * a * (1.0f + tanh_approx(0.7978845608f * fmaf(0.044715f * a, a * a, a)));
+    case 2: return 0.5f * a * (1.0f + erf_as7126(a * 0.70710678118654752f));
+    case 3: return __fdividef(a, 1.0f + __expf(-a));
+    default: return a;
+  }
+}
+
 // kActNone / kActGeluTanh / kActGeluErf / kActSilu (the enum of kernels.h).
 GBF_DEVICE float apply_act(float a, int act) {
   switch (act) {

@@ -27,12 +27,6 @@ namespace {
 constexpr int kGaBlock = 256;
 constexpr int kGaUnroll = 4;
 
-GBF_DEVICE float tanh_approx(float a) {
-  float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(a));
-  return t;
-}
-
 template <int ACT>
 GBF_DEVICE float gate_act(float a) {
   if (ACT == kActSilu) return __fdividef(a, 1.0f + __expf(-a));

@@ -20,9 +20,10 @@
 //   warp 2     allocates (and at exit frees) 512 TMEM columns: two 128 x 256
 //              float32 accumulators, so the epilogue of tile i overlaps the
 //              MMAs of tile i + 1.
-//   warps 4-7  epilogue: tcgen05.ld 32 columns at a time (warp w reads TMEM
-//              lanes 32 (w % 4) .. +31, one output row per thread), add bias,
-//              GELU, round to bf16, 16-byte stores.
+//   warps 4-11 epilogue: tcgen05.ld 32 columns at a time (warp w reads TMEM
+//              lanes 32 (w % 4) .. +31, one output row per thread, half of
+//              the tile's columns), descales and bias, the activation (fast
+//              forms, see common.cuh), round to bf16, 16-byte stores.
 // Tile order: the N tiles are cut into groups of kGroupN; inside a group the
 // tiles run n-fastest, so the CTAs working at one time cover about ten 128-row
 // blocks of X against the group's kGroupN W column blocks.  A group's W
@@ -51,8 +52,9 @@ constexpr int A_STAGE_BYTES = BM * BK_BYTES;     // 16 KB
 constexpr int B_STAGE_BYTES = BN * BK_BYTES;     // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;                // two accumulators
-constexpr int kThreads = 256;
-constexpr int kEpilogueWarp0 = 4;
+constexpr int kThreads = 384;
+constexpr int kEpilogueWarp0 = 4;                // warps 4..11: two per TMEM lane quarter
+constexpr int kEpilogueWarps = 8;
 
 struct __align__(8) SharedCtl {
   uint64_t full[STAGES];
@@ -75,12 +77,45 @@ GBF_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, in
       : "memory");
 }
 
+// The same load delivered to the same shared-memory offset of every CTA in
+// `mask` (bit i = CTA rank i of the cluster), completing on the mbarrier at
+// the same offset in each of them.
+GBF_DEVICE void tma_load_2d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                      uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
+      : "memory");
+}
+
+GBF_DEVICE uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster: release this CTA's prior memory
+// operations and wait for all of the cluster's threads.
+GBF_DEVICE void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 GBF_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 GBF_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 GBF_DEVICE void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// tc_commit arriving on the mbarrier at the same offset in every CTA of `mask`.
+GBF_DEVICE void tc_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+      ::"r"(smem_u32(bar)), "h"(mask)
+      : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T with a float32 accumulator: kind::f16 for
@@ -151,23 +186,32 @@ struct GemmParams {
   int act;
 };
 
-// Output tile origin (m0, n0) of linear tile index `tile` (see the tile order above).
-GBF_DEVICE void tile_origin(const GemmParams& p, int tile, int& m0, int& n0) {
-  const int per_group = kGroupN * p.m_tiles;
+// Output tile origin (m0, n0) of linear work index `tile` (see the tile order
+// above).  With clusters of CL CTAs a work item is CL vertically adjacent M
+// tiles sharing one W column block: m_units = ceil(m_tiles / CL), and CTA rank
+// `rank` of the cluster takes M tile unit * CL + rank.
+GBF_DEVICE void tile_origin(const GemmParams& p, int m_units, int cl, int rank, int tile, int& m0, int& n0) {
+  const int per_group = kGroupN * m_units;
   const int g = tile / per_group;
   const int idx = tile - g * per_group;
   const int n_base = g * kGroupN;
   const int gs = p.n_tiles - n_base < kGroupN ? p.n_tiles - n_base : kGroupN;
-  m0 = (idx / gs) * BM;
+  m0 = ((idx / gs) * cl + rank) * BM;
   n0 = (n_base + idx % gs) * BN;
 }
 
-template <bool FP8>
+// CL = 1: one CTA per work item.  CL = 2: clusters of two CTAs on vertically
+// adjacent M tiles; each CTA loads its own X tile and half of the shared W
+// tile, multicast to both, so each SM pulls 32 KB instead of 48 KB per
+// k-block; a stage is free again once both CTAs' MMAs have read it (each
+// MMA issuer's commit arrives on the stage's empty barrier in both CTAs).
+template <bool FP8, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                         const GemmParams p) {
   constexpr int BK = FP8 ? BK_BYTES : BK_BYTES / 2;         // K elements per k-block
   constexpr uint32_t kIdesc = FP8 ? kIdescE4m3 : kIdescBf16;
+  constexpr uint16_t kPair = 0x3;                            // both CTAs of a two-CTA cluster
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smem_a = smem;                                   // STAGES x 16 KB
@@ -176,17 +220,20 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = p.m_tiles * p.n_tiles;
+  const int rank = CL == 1 ? 0 : static_cast<int>(cluster_ctarank());
+  const int m_units = (p.m_tiles + CL - 1) / CL;
+  const int num_tiles = m_units * p.n_tiles;
+  const int first = blockIdx.x / CL, stride = gridDim.x / CL;
   const int k_blocks = p.k / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], 1);
+      mbar_init(&ctl->empty[s], CL);       // one commit from each CTA's MMA issuer
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctl->tmem_full[a], 1);
-      mbar_init(&ctl->tmem_empty[a], 4);     // one arrive per epilogue warp
+      mbar_init(&ctl->tmem_empty[a], kEpilogueWarps);     // one arrive per epilogue warp
     }
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -202,6 +249,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();              // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
@@ -212,9 +260,9 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       uint32_t phase = 0;
       uint32_t issued[STAGES] = {};        // phases issued per stage (for the final drain)
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = first; tile < num_tiles && ok; tile += stride) {
         int m0, n0;
-        tile_origin(p, tile, m0, n0);
+        tile_origin(p, m_units, CL, rank, tile, m0, n0);
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, &ctl->abort, p.err)) {
             ok = false;
@@ -222,7 +270,11 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
           }
           mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
           tma_load_2d(smem_a + stage * A_STAGE_BYTES, &map_x, &ctl->full[stage], kb * BK, m0);
-          tma_load_2d(smem_b + stage * B_STAGE_BYTES, &map_w, &ctl->full[stage], kb * BK, n0);
+          if (CL == 1)
+            tma_load_2d(smem_b + stage * B_STAGE_BYTES, &map_w, &ctl->full[stage], kb * BK, n0);
+          else
+            tma_load_2d_multicast(smem_b + stage * B_STAGE_BYTES + rank * (B_STAGE_BYTES / 2), &map_w,
+                                  &ctl->full[stage], kb * BK, n0 + rank * (BN / 2), kPair);
           ++issued[stage];
           if (++stage == STAGES) {
             stage = 0;
@@ -243,7 +295,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       uint32_t phase = 0;
       bool ok = true;
       int local = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+      for (int tile = first; tile < num_tiles && ok; tile += stride, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1u;
         if (!mbar_wait(&ctl->tmem_empty[acc], acc_phase ^ 1u, &ctl->abort, p.err)) break;
@@ -264,7 +316,10 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
             const uint64_t b_desc = smem_desc_sw128(b_addr + kk * UMMA_K_BYTES);
             tc_mma<FP8>(d_tmem, a_desc, b_desc, kIdesc, (kb | kk) != 0);
           }
-          tc_commit(&ctl->empty[stage]);      // frees the stage once these MMAs have read it
+          if (CL == 1)
+            tc_commit(&ctl->empty[stage]);      // frees the stage once these MMAs have read it
+          else
+            tc_commit_multicast(&ctl->empty[stage], kPair);   // ... in both CTAs of the cluster
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -279,9 +334,10 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
     }
   } else if (warp >= kEpilogueWarp0) {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp - kEpilogueWarp0;          // TMEM lanes 32*quarter .. +31
+    const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31 (warp % 4)
+    const int half = (warp - kEpilogueWarp0) >> 2;      // columns 128*half .. +127 of the tile
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int tile = first; tile < num_tiles; tile += stride, ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1u;
       bool ok = true;
@@ -290,12 +346,12 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       if (!ok) break;
       tc_fence_after();
       int m0, n0;
-      tile_origin(p, tile, m0, n0);
+      tile_origin(p, m_units, CL, rank, tile, m0, n0);
       const int row = m0 + quarter * 32 + lane;
       __nv_bfloat16* yrow = p.y + static_cast<int64_t>(row) * p.n;
       const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
         uint32_t r[32];
         tmem_ld_32cols(taddr + c * 32, r);
         const int col0 = n0 + c * 32;
@@ -318,7 +374,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
           for (int e = 0; e < 8; ++e) {
             const float acc = __uint_as_float(r[g * 8 + e]);
             const float a = FP8 ? fmaf(acc, sc[e], bz[e]) : acc + bz[e];
-            v[e] = apply_act(a, p.act);
+            v[e] = fast_act(a, p.act);
           }
           if (row < p.m) st_16(yrow + col, f32x8_to_bf16x8(v));
         }
@@ -331,6 +387,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
 
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();              // no multicast or remote arrive is left in flight to this CTA
   if (warp == 2) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
@@ -375,12 +432,40 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <bool FP8, int CL>
+cudaError_t launch_gemm(const CUtensorMap& map_x, const CUtensorMap& map_w, const GemmParams& p, int sms,
+                        cudaStream_t stream, const char** why) {
+  auto kern = linear_bias_gelu_kernel<FP8, CL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) {
+    *why = "could not reserve shared memory";
+    return e;
+  }
+  const int units = ((p.m_tiles + CL - 1) / CL) * p.n_tiles;
+  const int slots = sms / CL;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((units < slots ? units : slots) * CL));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, map_x, map_w, p);
+}
+
 }  // namespace
 
 cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, const char** why) {
-  CUtensorMap map_x, map_w;
   const bool fp8 = a.fp8 != 0;
-  if (!make_map(&map_x, a.x, a.m, a.k, BM, fp8) || !make_map(&map_w, a.w, a.n, a.k, BN, fp8)) {
+  const int m_tiles = static_cast<int>((a.m + BM - 1) / BM);
+  const int cl = m_tiles >= 2 ? 2 : 1;                  // two-CTA clusters share W tiles
+  CUtensorMap map_x, map_w;
+  if (!make_map(&map_x, a.x, a.m, a.k, BM, fp8) || !make_map(&map_w, a.w, a.n, a.k, BN / cl, fp8)) {
     *why = "cuTensorMapEncodeTiled is unavailable or rejected the operands";
     return cudaErrorInvalidValue;
   }
@@ -393,21 +478,20 @@ cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, cons
   p.m = static_cast<int>(a.m);
   p.n = static_cast<int>(a.n);
   p.k = static_cast<int>(a.k);
-  p.m_tiles = static_cast<int>((a.m + BM - 1) / BM);
+  p.m_tiles = m_tiles;
   p.n_tiles = static_cast<int>((a.n + BN - 1) / BN);
   p.act = a.act;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int tiles = p.m_tiles * p.n_tiles;
-  const int grid = tiles < sms ? tiles : sms;
-  auto kern = fp8 ? linear_bias_gelu_kernel<true> : linear_bias_gelu_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) {
-    *why = "could not reserve shared memory";
-    return e;
-  }
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(map_x, map_w, p);
+  cudaError_t e;
+  if (fp8)
+    e = cl == 2 ? launch_gemm<true, 2>(map_x, map_w, p, sms, stream, why)
+                : launch_gemm<true, 1>(map_x, map_w, p, sms, stream, why);
+  else
+    e = cl == 2 ? launch_gemm<false, 2>(map_x, map_w, p, sms, stream, why)
+                : launch_gemm<false, 1>(map_x, map_w, p, sms, stream, why);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
