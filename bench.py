@@ -490,7 +490,7 @@ def build_ops(gbf, with_gemm, only=None, small=False):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """SM clock, power and throttle reasons sampled every 10 ms while the timed
+    """SM and memory clocks, power and throttle reasons sampled every 10 ms while the timed
     region runs, read from NVML (libnvidia-ml, through ctypes); falls back to
     nvidia-smi at 50 ms when NVML cannot be loaded."""
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
@@ -499,6 +499,7 @@ class ClockSampler:
     def __init__(self, cuda_index):
         self.cuda_index = cuda_index
         self.samples, self.first, self.stop_flag = [], 0, False
+        self.mem_mhz = []
         self.nvml, self.dev, self.max_mhz, self.thread, self.proc = None, None, None, None, None
 
     def _open_nvml(self):
@@ -522,12 +523,14 @@ class ClockSampler:
 
     def _poll(self):
         import ctypes
-        clk, rea, pw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        clk, mclk, rea, pw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
         while not self.stop_flag:
-            self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk))
+            self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk))      # NVML_CLOCK_SM
+            self.nvml.nvmlDeviceGetClockInfo(self.dev, 2, ctypes.byref(mclk))     # NVML_CLOCK_MEM
             self.reasons_fn(self.dev, ctypes.byref(rea))
             self.nvml.nvmlDeviceGetPowerUsage(self.dev, ctypes.byref(pw))
             self.samples.append((float(clk.value), int(rea.value), pw.value / 1000.0))
+            self.mem_mhz.append(float(mclk.value))
             time.sleep(0.01)
 
     def start(self):
@@ -578,10 +581,14 @@ class ClockSampler:
             for bit, name in self.REASONS.items():
                 if r & bit:
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(c for c, _, _ in got), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(reasons), "samples": len(got),
-                "power_w_max": round(max(p for _, _, p in got), 1),
-                "source": "nvml" if self.thread is not None else "nvidia-smi"}
+        out = {"sm_mhz": statistics.median(c for c, _, _ in got), "sm_max_mhz": self.max_mhz,
+               "reasons": sorted(reasons), "samples": len(got),
+               "power_w_max": round(max(p for _, _, p in got), 1),
+               "source": "nvml" if self.thread is not None else "nvidia-smi"}
+        mem = self.mem_mhz[self.first:]
+        if mem:
+            out["mem_mhz"] = statistics.median(mem)
+        return out
 
 
 # ------------------------------------------------------------- traffic record
@@ -769,6 +776,26 @@ def sum_over_ranks(pg, v):
     return float(t.item())
 
 
+def copy_probe_gbs(gbf, nbytes=1 << 30, reps=10):
+    """Best of `reps` event-timed gbf_copy calls of 1 GiB (read + write bytes
+    per second): this library's own copy-kernel bandwidth, reported beside the
+    measured peak the fractions use."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    src.fill_(1)
+    dst = torch.empty_like(src)
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        gbf.copy(src, dst)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del src, dst
+    return round(2 * nbytes / (best / 1e3) / 1e9, 1)
+
+
 def main_gpu(args):
     import torch
     world, rank, local, pg = dist_setup(args.gpus)
@@ -870,6 +897,10 @@ def main_gpu(args):
                        "l2": "flushed (512 MB write, then read back) before every operator, outside its event pair",
                        "value_scope": "memory-bound fused kernels; GEMM timed in the same step, see ops"},
             "roofline": roofline, "ops": out_ops, "clocks": clk,
+            "peaks": {"hbm_gbs_measured_copy": peaks["hbm_gbs"], "bf16_tflops_measured": peaks["bf16_tflops"],
+                      "source": peaks["source"], "hbm_gbs_nominal": 7900.0, "bf16_tflops_dense_nominal": 2250.0,
+                      "nominal_source": "GB300 nominal figures (HBM3e 7.9 TB/s; dense bf16 2.25 PFLOP/s)",
+                      "gbf_copy_gbs": copy_probe_gbs(gbf)},
             "latency_bound": {n: {"us_per_launch": round(d["ms"] * 1e3 / d["launches"], 3), "launches": d["launches"]}
                               for n, d in out_ops.items()
                               if "gbs" in d and per_op[n]["op"].algorithmic_bytes() // per_op[n]["op"].launches < (1 << 20)},
