@@ -157,9 +157,12 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
       for (int h0 = grp; h0 < heads; h0 += kRotBatch * kRotGroups) {
         if (h0 != grp) load_batch(h0);
 #pragma unroll
-        for (int u = 0; u < kRotBatch; ++u) {
+        // last head of the batch first: V heads come last in the row, and
+        // copying them out first frees their registers for the norm work
+        for (int uu = 0; uu < kRotBatch; ++uu) {
+          const int u = kRotBatch - 1 - uu;
           const int h = h0 + u * kRotGroups;
-          if (h >= heads) break;
+          if (h >= heads) continue;
           if (h >= a.n_q + a.n_kv) {               // V: pass through
             if (slot_ok) {
               __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.v_cache) +
@@ -217,15 +220,15 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
               m1 = fma_bf16_hi(xh[i], kOnes, m1);
             }
             const float mean = segment_sum(m0 + m1, LPH) * (1.0f / static_cast<float>(D));
-            float cl[8], ch[8], v0 = 0.f, v1 = 0.f;
+            // centred values are formed again in the output pass (one FMA each)
+            // rather than held in registers across it
+            float v0 = 0.f, v1 = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              cl[2 * i] = fma_bf16_lo(xl[i], kOnes, -mean);
-              cl[2 * i + 1] = fma_bf16_hi(xl[i], kOnes, -mean);
-              ch[2 * i] = fma_bf16_lo(xh[i], kOnes, -mean);
-              ch[2 * i + 1] = fma_bf16_hi(xh[i], kOnes, -mean);
-              v0 = fmaf(cl[2 * i], cl[2 * i], fmaf(ch[2 * i], ch[2 * i], v0));
-              v1 = fmaf(cl[2 * i + 1], cl[2 * i + 1], fmaf(ch[2 * i + 1], ch[2 * i + 1], v1));
+              const float c0 = fma_bf16_lo(xl[i], kOnes, -mean), c1 = fma_bf16_hi(xl[i], kOnes, -mean);
+              const float c2h = fma_bf16_lo(xh[i], kOnes, -mean), c3 = fma_bf16_hi(xh[i], kOnes, -mean);
+              v0 = fmaf(c0, c0, fmaf(c2h, c2h, v0));
+              v1 = fmaf(c1, c1, fmaf(c3, c3, v1));
             }
             const float var = segment_sum(v0 + v1, LPH) * (1.0f / static_cast<float>(D));
             const bool is_q = h < a.n_q;
@@ -243,8 +246,10 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const float2 inv2 = make_float2(inv, inv);
-              const float2 ul = __ffma2_rn(__fmul2_rn(make_float2(cl[2 * i], cl[2 * i + 1]), inv2), pair(wl[i]), pair(bl[i]));
-              const float2 uh = __ffma2_rn(__fmul2_rn(make_float2(ch[2 * i], ch[2 * i + 1]), inv2), pair(wh[i]), pair(bh[i]));
+              const float2 cl2 = make_float2(fma_bf16_lo(xl[i], kOnes, -mean), fma_bf16_hi(xl[i], kOnes, -mean));
+              const float2 ch2 = make_float2(fma_bf16_lo(xh[i], kOnes, -mean), fma_bf16_hi(xh[i], kOnes, -mean));
+              const float2 ul = __ffma2_rn(__fmul2_rn(cl2, inv2), pair(wl[i]), pair(bl[i]));
+              const float2 uh = __ffma2_rn(__fmul2_rn(ch2, inv2), pair(wh[i]), pair(bh[i]));
               const float2 rl = __ffma2_rn(ul, c2[i], __fmul2_rn(make_float2(-s2[i].x, -s2[i].y), uh));
               const float2 rh = __ffma2_rn(uh, c2[i], __fmul2_rn(s2[i], ul));
               ol[i] = f32x2_to_bf16x2(rl.x, rl.y);
