@@ -434,7 +434,8 @@ GBF_API int gbf_device_status(void* stream) {
   }
   if (word & gbf::DEV_ERR_MBAR_TIMEOUT)
     return fail(GBF_ETIMEOUT, "gbf_device_status: a bounded wait inside a kernel gave up (word 0x%x)", word);
-  if (word) return fail(GBF_EDEVICE, "gbf_device_status: device fault word 0x%x (bit 0: cache slot out of range)", word);
+  if (word) return fail(GBF_EDEVICE, "gbf_device_status: device fault word 0x%x (bit 0: cache slot out of range; "
+                         "bit 2: a GEMM CTA pair got different TMEM bases)", word);
   return ok();
 }
 

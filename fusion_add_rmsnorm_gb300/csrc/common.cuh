@@ -20,6 +20,7 @@ namespace gbf {
 enum : unsigned int {
   DEV_ERR_SLOT_RANGE = 1u << 0,    // a KV-cache slot index was outside [0, cache_rows)
   DEV_ERR_MBAR_TIMEOUT = 1u << 1,  // a bounded mbarrier wait gave up
+  DEV_ERR_PAIR_TMEM = 1u << 2,     // the two CTAs of a tensor-core pair got different TMEM bases
 };
 
 GBF_DEVICE void raise_error(unsigned int* err, unsigned int bit) {
@@ -153,16 +154,22 @@ GBF_DEVICE float act_silu(float a) { return a / (1.0f + expf(-a)); }
 //    error below 2^-10.9);
 //  * erf GELU with erf(x) = 1 - (a1 t + ... + a5 t^5) e^(-x^2), t = 1/(1 + p x)
 //    for x >= 0 (M. Abramowitz, I. Stegun, "Handbook of Mathematical
-//    Functions", 1964, formula 7.1.26; absolute error below 1.5e-7), odd in x;
+//    Functions", 1964, formula 7.1.26; absolute error below 1.5e-7), odd in x,
+//    with t from the hardware reciprocal approximation (rcp.approx, 1 ulp);
 //  * SiLU with the fast exponential and division intrinsics.
 GBF_DEVICE float tanh_approx(float a) {
   float t;
   asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(a));
   return t;
 }
+GBF_DEVICE float rcp_approx(float a) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+  return r;
+}
 GBF_DEVICE float erf_as7126(float x) {
   const float ax = fabsf(x);
-  const float t = __frcp_rn(fmaf(0.3275911f, ax, 1.0f));
+  const float t = rcp_approx(fmaf(0.3275911f, ax, 1.0f));   // argument >= 1: no subnormal or zero
   float poly = fmaf(1.061405429f, t, -1.453152027f);
   poly = fmaf(poly, t, 1.421413741f);
   poly = fmaf(poly, t, -0.284496736f);

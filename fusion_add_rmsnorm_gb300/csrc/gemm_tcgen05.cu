@@ -9,21 +9,36 @@
 // MatMul -> BiasAdd -> activation pattern of the CANN graph-autofusion article
 // (three HBM passes become one); npu_linear of the MindIE-SD RFC, §3.5.
 //
-// Design (one CTA per SM, persistent):
-//   tiles      BM x BN = 128 x 256 output tile, BK = 64 (one 128-byte swizzle
-//              row of bf16), four tcgen05.mma of M128 N256 K16 per k-block.
-//   warp 0     TMA producer: cp.async.bulk.tensor 2D loads of the X and W
-//              k-blocks into a 4-stage shared-memory ring (128-byte swizzle).
-//   warp 1     MMA issuer: one elected thread issues tcgen05.mma from shared
-//              memory descriptors into a TMEM accumulator and commits each
-//              stage back to the producer with tcgen05.commit.
+// Design (persistent, one CTA per SM; CTA pairs when M spans two tiles):
+//   tiles      each CTA owns a BM x BN = 128 x 256 output tile; BK = one
+//              128-byte swizzle row of K (64 bf16 or 128 E4M3) per k-block.
+//   pairs      a cluster of two CTAs on vertically adjacent M tiles runs as
+//              one tcgen05 CTA pair (cta_group::2): the even CTA issues
+//              M256 N256 MMAs that read X rows from both CTAs' shared memory
+//              and W rows 0..127 of the tile from its own, 128..255 from the
+//              other's, writing each CTA's 128 x 256 accumulator into that
+//              CTA's TMEM.  Each SM stages 32 KB per k-block instead of 48 KB,
+//              which is what bounds a single CTA's MMA rate (shared-memory
+//              bandwidth: TMA writes plus operand reads).  A single M tile
+//              runs unpaired (cta_group::1, M128 N256).
+//   warp 0     TMA producer (each CTA): cp.async.bulk.tensor 2D loads of its
+//              X and W k-blocks into a shared-memory ring (128-byte swizzle);
+//              in a pair both CTAs' copies complete on the even CTA's
+//              barrier, which expects the bytes of both.
+//   warp 1     MMA issuer (the even CTA of a pair): one elected thread issues
+//              tcgen05.mma from shared-memory descriptors into TMEM and
+//              commits each stage back to both CTAs' producers.
 //   warp 2     allocates (and at exit frees) 512 TMEM columns: two 128 x 256
 //              float32 accumulators, so the epilogue of tile i overlaps the
 //              MMAs of tile i + 1.
-//   warps 4-11 epilogue: tcgen05.ld 32 columns at a time (warp w reads TMEM
-//              lanes 32 (w % 4) .. +31, one output row per thread, half of
-//              the tile's columns), descales and bias, the activation (fast
-//              forms, see common.cuh), round to bf16, 16-byte stores.
+//   warps 4-11 epilogue (each CTA): tcgen05.ld 32 columns at a time (warp w
+//              reads TMEM lanes 32 (w % 4) .. +31, one output row per thread,
+//              half of the tile's columns), descales and bias, the activation
+//              (fast forms, see common.cuh), round to bf16; a 4 x 4 shuffle
+//              transpose inside each lane quad turns the one-row-per-lane
+//              layout into stores of 8 rows x 64 contiguous bytes;
+//              then the warp arrives on the even CTA's "accumulator free"
+//              barrier.
 // Tile order: the N tiles are cut into groups of kGroupN; inside a group the
 // tiles run n-fastest, so the CTAs working at one time cover about ten 128-row
 // blocks of X against the group's kGroupN W column blocks.  A group's W
@@ -33,8 +48,9 @@
 // Every mbarrier wait is bounded (about one second of wall time): a wait that
 // gives up sets DEV_ERR_MBAR_TIMEOUT in the device error word and raises a
 // CTA-wide abort flag; every role then leaves its loop, the MMA issuer drains
-// its outstanding tensor-core work, the producer waits (bounded) for its
-// in-flight copies, and TMEM is freed before the CTA exits.
+// its outstanding tensor-core work, the producers' copies are all waited for
+// (bounded), and TMEM is freed before the CTAs exit.  No role returns early:
+// both CTAs of a pair always reach the closing cluster barriers.
 #include <cuda.h>
 
 #include "kernels.h"
@@ -43,30 +59,43 @@
 namespace gbf {
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = 128;                          // output rows per CTA (TMEM lanes)
 constexpr int BN = 256;
 constexpr int BK_BYTES = 128;                    // one 128-byte swizzle row of K per k-block
 constexpr int UMMA_K_BYTES = 32;                 // K of one MMA: 16 bf16 or 32 E4M3 values
-constexpr int STAGES = 4;
 constexpr int A_STAGE_BYTES = BM * BK_BYTES;     // 16 KB
-constexpr int B_STAGE_BYTES = BN * BK_BYTES;     // 32 KB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int TMEM_COLS = 2 * BN;                // two accumulators
+constexpr int TMEM_COLS = 2 * BN;                // two accumulators (all 512 columns)
 constexpr int kThreads = 384;
 constexpr int kEpilogueWarp0 = 4;                // warps 4..11: two per TMEM lane quarter
 constexpr int kEpilogueWarps = 8;
 
+// Shared-memory ring of one CTA: unpaired, the whole W tile per stage; paired,
+// half of it (the other half sits in the other CTA).
+template <bool PAIR>
+struct Ring {
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;
+  static constexpr int kBStageBytes = kBRows * BK_BYTES;
+  static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes;
+};
+
+template <int S>
 struct __align__(8) SharedCtl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[S];
+  uint64_t empty[S];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
+  uint32_t peer_issued[S];   // pair, even CTA: k-blocks the odd CTA issued per stage
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + sizeof(SharedCtl);
+template <bool PAIR>
+constexpr size_t smem_bytes() {
+  return 1024 /* alignment slack */ + Ring<PAIR>::kStages * Ring<PAIR>::kStageBytes +
+         sizeof(SharedCtl<Ring<PAIR>::kStages>);
+}
 
 // ------------------------------------------------------------ PTX wrappers
 
@@ -77,15 +106,13 @@ GBF_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, in
       : "memory");
 }
 
-// The same load delivered to the same shared-memory offset of every CTA in
-// `mask` (bit i = CTA rank i of the cluster), completing on the mbarrier at
-// the same offset in each of them.
-GBF_DEVICE void tma_load_2d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
-                                      uint16_t mask) {
+// A load into this CTA's shared memory completing on an mbarrier that may sit
+// in either CTA of the pair (`bar` is a shared::cluster address).
+GBF_DEVICE void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
 
@@ -93,6 +120,35 @@ GBF_DEVICE uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
+}
+
+// shared::cluster address of the object at this CTA's shared address `a`, in
+// CTA `rank` of the cluster.
+GBF_DEVICE uint32_t map_cluster(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+GBF_DEVICE uint32_t ld_cluster_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+GBF_DEVICE void st_cluster_u32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address).
+GBF_DEVICE void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Count `bytes` of the current phase's expected transactions as done.
+GBF_DEVICE void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
 }
 
 // Every thread of every CTA of the cluster: release this CTA's prior memory
@@ -105,38 +161,88 @@ GBF_DEVICE void cluster_sync() {
 GBF_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 GBF_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-GBF_DEVICE void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
+// Every tcgen05 instruction of one kernel names the same CTA group: 1 when
+// unpaired, 2 in a pair.
+template <bool PAIR>
+GBF_DEVICE void tmem_alloc(uint32_t* dst) {
+  if (PAIR) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
 }
 
-// tc_commit arriving on the mbarrier at the same offset in every CTA of `mask`.
-GBF_DEVICE void tc_commit_multicast(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-      ::"r"(smem_u32(bar)), "h"(mask)
-      : "memory");
+template <bool PAIR>
+GBF_DEVICE void tmem_dealloc(uint32_t base) {
+  if (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(TMEM_COLS) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(TMEM_COLS) : "memory");
+}
+
+// Arrive on `bar` once the tensor-core work issued so far has completed:
+// unpaired, in this CTA; paired, at the same offset in both CTAs.
+template <bool PAIR>
+GBF_DEVICE void tc_commit(uint64_t* bar) {
+  if (PAIR)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"(static_cast<uint16_t>(0x3))
+        : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// tc_commit arriving on this CTA's `bar` only (the issuer's final drain).
+template <bool PAIR>
+GBF_DEVICE void tc_commit_self(uint64_t* bar) {
+  if (PAIR)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T with a float32 accumulator: kind::f16 for
 // bf16 operands, kind::f8f6f4 for E4M3 operands (both operands one type).
-template <bool FP8>
+template <bool FP8, bool PAIR>
 GBF_DEVICE void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
-  if (FP8) {
+  if (FP8 && PAIR)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else if (FP8)
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
-  } else {
+  else if (PAIR)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
-  }
 }
 
 // 32 consecutive float32 columns of this warp's 32 TMEM lanes, one lane per thread.
@@ -151,6 +257,33 @@ GBF_DEVICE void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+GBF_DEVICE uint4 shfl_xor_u4(uint4 v, int m) {
+  v.x = __shfl_xor_sync(0xffffffffu, v.x, m);
+  v.y = __shfl_xor_sync(0xffffffffu, v.y, m);
+  v.z = __shfl_xor_sync(0xffffffffu, v.z, m);
+  v.w = __shfl_xor_sync(0xffffffffu, v.w, m);
+  return v;
+}
+
+// 4 x 4 transpose of 16-byte pieces inside each group of four lanes: on entry
+// lane 4q + i holds pieces 0..3 of its own row; on exit it holds piece i of
+// rows 4q + 0..3.  Two exchange rounds: the off-diagonal 2 x 2 blocks with
+// lane ^ 2, then the off-diagonal pieces inside each block with lane ^ 1.
+GBF_DEVICE void quad_transpose(uint4 (&pc)[4], int i) {
+  const bool hi2 = (i & 2) != 0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint4 r = shfl_xor_u4(hi2 ? pc[j] : pc[j + 2], 2);
+    if (hi2) pc[j] = r; else pc[j + 2] = r;
+  }
+  const bool hi1 = (i & 1) != 0;
+#pragma unroll
+  for (int j = 0; j < 4; j += 2) {
+    const uint4 r = shfl_xor_u4(hi1 ? pc[j] : pc[j + 1], 1);
+    if (hi1) pc[j] = r; else pc[j + 1] = r;
+  }
 }
 
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the
@@ -168,10 +301,11 @@ GBF_DEVICE uint64_t smem_desc_sw128(uint32_t addr) {
 
 // Instruction descriptors: float32 D (bits 4-5 = 1), A and B type codes at
 // bits 7-9 and 10-12 (kind::f16: bf16 = 1; kind::f8f6f4: E4M3 = 0), both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t kIdescShape = (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
-constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | kIdescShape;
-constexpr uint32_t kIdescE4m3 = (1u << 4) | (0u << 7) | (0u << 10) | kIdescShape;
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24 (M = 256 for a CTA pair).
+__host__ __device__ constexpr uint32_t idesc(bool fp8, int m) {
+  return (1u << 4) | ((fp8 ? 0u : 1u) << 7) | ((fp8 ? 0u : 1u) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
 
 constexpr int kGroupN = 16;
 
@@ -187,9 +321,9 @@ struct GemmParams {
 };
 
 // Output tile origin (m0, n0) of linear work index `tile` (see the tile order
-// above).  With clusters of CL CTAs a work item is CL vertically adjacent M
-// tiles sharing one W column block: m_units = ceil(m_tiles / CL), and CTA rank
-// `rank` of the cluster takes M tile unit * CL + rank.
+// above).  With CTA pairs a work item is two vertically adjacent M tiles
+// sharing one W column block: m_units = ceil(m_tiles / cl), and CTA rank
+// `rank` of the pair takes M tile unit * cl + rank.
 GBF_DEVICE void tile_origin(const GemmParams& p, int m_units, int cl, int rank, int tile, int& m0, int& n0) {
   const int per_group = kGroupN * m_units;
   const int g = tile / per_group;
@@ -200,40 +334,40 @@ GBF_DEVICE void tile_origin(const GemmParams& p, int m_units, int cl, int rank, 
   n0 = (n_base + idx % gs) * BN;
 }
 
-// CL = 1: one CTA per work item.  CL = 2: clusters of two CTAs on vertically
-// adjacent M tiles; each CTA loads its own X tile and half of the shared W
-// tile, multicast to both, so each SM pulls 32 KB instead of 48 KB per
-// k-block; a stage is free again once both CTAs' MMAs have read it (each
-// MMA issuer's commit arrives on the stage's empty barrier in both CTAs).
-template <bool FP8, int CL>
+template <bool FP8, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                         const GemmParams p) {
+  using R = Ring<PAIR>;
+  constexpr int S = R::kStages;
+  constexpr int CL = PAIR ? 2 : 1;
   constexpr int BK = FP8 ? BK_BYTES : BK_BYTES / 2;         // K elements per k-block
-  constexpr uint32_t kIdesc = FP8 ? kIdescE4m3 : kIdescBf16;
-  constexpr uint16_t kPair = 0x3;                            // both CTAs of a two-CTA cluster
+  constexpr uint32_t kIdesc = idesc(FP8, CL * BM);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the same offsets in both CTAs of a pair: the MMAs address the odd CTA's
+  // operands by the even CTA's shared addresses
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* smem_a = smem;                                   // STAGES x 16 KB
-  uint8_t* smem_b = smem + STAGES * A_STAGE_BYTES;          // STAGES x 32 KB
-  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* smem_a = smem;                                   // S x 16 KB
+  uint8_t* smem_b = smem + S * A_STAGE_BYTES;               // S x (32 or 16) KB
+  SharedCtl<S>* ctl = reinterpret_cast<SharedCtl<S>*>(smem + S * R::kStageBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rank = CL == 1 ? 0 : static_cast<int>(cluster_ctarank());
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;            // issues the MMAs (always, unpaired)
   const int m_units = (p.m_tiles + CL - 1) / CL;
-  const int num_tiles = m_units * p.n_tiles;
   const int first = blockIdx.x / CL, stride = gridDim.x / CL;
   const int k_blocks = p.k / BK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], CL);       // one commit from each CTA's MMA issuer
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&ctl->full[s], 1);         // the even CTA's expect-bytes arrive
+      mbar_init(&ctl->empty[s], 1);        // the MMA issuer's commit
+      ctl->peer_issued[s] = 0;
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctl->tmem_full[a], 1);
-      mbar_init(&ctl->tmem_empty[a], kEpilogueWarps);     // one arrive per epilogue warp
+      mbar_init(&ctl->tmem_empty[a], CL * kEpilogueWarps);   // one arrive per epilogue warp of the pair
     }
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -241,56 +375,62 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
   }
-  if (warp == 2) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&ctl->tmem_base)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
+  if (warp == 2) tmem_alloc<PAIR>(&ctl->tmem_base);
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();              // the peer's barriers exist before any multicast reaches them
+  if (PAIR) cluster_sync();                // both CTAs' barriers and TMEM exist before either is used
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  // The pair's MMAs address both CTAs' accumulators by one TMEM address; the
+  // whole of TMEM is allocated, so both bases are column 0 -- checked, and on
+  // a mismatch (both CTAs see it) the pair does no work and reports it.
+  bool usable = true;
+  if (PAIR) {
+    usable = ld_cluster_u32(map_cluster(smem_u32(&ctl->tmem_base), static_cast<uint32_t>(rank ^ 1))) == tmem_base;
+    if (!usable && threadIdx.x == 0) raise_error(p.err, DEV_ERR_PAIR_TMEM);
+  }
+  const int num_tiles = usable ? m_units * p.n_tiles : 0;
+
+  uint32_t issued[S];                      // producer: k-blocks issued per stage (for the final drain)
+#pragma unroll
+  for (int s = 0; s < S; ++s) issued[s] = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued[STAGES] = {};        // phases issued per stage (for the final drain)
       bool ok = true;
       for (int tile = first; tile < num_tiles && ok; tile += stride) {
         int m0, n0;
         tile_origin(p, m_units, CL, rank, tile, m0, n0);
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, &ctl->abort, p.err)) {
+          if (!mbar_wait<PAIR, false>(&ctl->empty[stage], phase ^ 1u, &ctl->abort, p.err)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
-          tma_load_2d(smem_a + stage * A_STAGE_BYTES, &map_x, &ctl->full[stage], kb * BK, m0);
-          if (CL == 1)
-            tma_load_2d(smem_b + stage * B_STAGE_BYTES, &map_w, &ctl->full[stage], kb * BK, n0);
-          else
-            tma_load_2d_multicast(smem_b + stage * B_STAGE_BYTES + rank * (B_STAGE_BYTES / 2), &map_w,
-                                  &ctl->full[stage], kb * BK, n0 + rank * (BN / 2), kPair);
+          if (leader) mbar_arrive_expect_tx(&ctl->full[stage], CL * R::kStageBytes);
+          if (PAIR) {
+            const uint32_t bar = map_cluster(smem_u32(&ctl->full[stage]), 0);
+            tma_load_2d_pair(smem_a + stage * A_STAGE_BYTES, &map_x, bar, kb * BK, m0);
+            tma_load_2d_pair(smem_b + stage * R::kBStageBytes, &map_w, bar, kb * BK, n0 + rank * R::kBRows);
+          } else {
+            tma_load_2d(smem_a + stage * A_STAGE_BYTES, &map_x, &ctl->full[stage], kb * BK, m0);
+            tma_load_2d(smem_b + stage * R::kBStageBytes, &map_w, &ctl->full[stage], kb * BK, n0);
+          }
           ++issued[stage];
-          if (++stage == STAGES) {
+          if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // Every issued copy has landed before the CTA may exit: wait for the
-      // last phase issued on each stage (bounded; immediate on the normal path).
-      int drain_abort = 0;                 // own flag: the CTA one may already be set
-      for (int s = 0; s < STAGES; ++s)
-        if (issued[s]) mbar_wait(&ctl->full[s], (issued[s] - 1) & 1u, &drain_abort, nullptr);
+      if (PAIR && !leader)                 // the even CTA drains the odd one's copies (they land on its barriers)
+        for (int s = 0; s < S; ++s) st_cluster_u32(map_cluster(smem_u32(&ctl->peer_issued[s]), 0), issued[s]);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -298,37 +438,34 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       for (int tile = first; tile < num_tiles && ok; tile += stride, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1u;
-        if (!mbar_wait(&ctl->tmem_empty[acc], acc_phase ^ 1u, &ctl->abort, p.err)) break;
+        if (!mbar_wait<PAIR, false>(&ctl->tmem_empty[acc], acc_phase ^ 1u, &ctl->abort, p.err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!mbar_wait(&ctl->full[stage], phase, &ctl->abort, p.err)) {
+          if (!mbar_wait<false, false>(&ctl->full[stage], phase, &ctl->abort, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem_a + stage * A_STAGE_BYTES);
-          const uint32_t b_addr = smem_u32(smem_b + stage * B_STAGE_BYTES);
+          const uint32_t b_addr = smem_u32(smem_b + stage * R::kBStageBytes);
 #pragma unroll
           for (int kk = 0; kk < BK_BYTES / UMMA_K_BYTES; ++kk) {
             // advance one MMA's K (32 bytes) inside the swizzled row
             const uint64_t a_desc = smem_desc_sw128(a_addr + kk * UMMA_K_BYTES);
             const uint64_t b_desc = smem_desc_sw128(b_addr + kk * UMMA_K_BYTES);
-            tc_mma<FP8>(d_tmem, a_desc, b_desc, kIdesc, (kb | kk) != 0);
+            tc_mma<FP8, PAIR>(d_tmem, a_desc, b_desc, kIdesc, (kb | kk) != 0);
           }
-          if (CL == 1)
-            tc_commit(&ctl->empty[stage]);      // frees the stage once these MMAs have read it
-          else
-            tc_commit_multicast(&ctl->empty[stage], kPair);   // ... in both CTAs of the cluster
-          if (++stage == STAGES) {
+          tc_commit<PAIR>(&ctl->empty[stage]);   // frees the stage (in both CTAs) once these MMAs have read it
+          if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) tc_commit(&ctl->tmem_full[acc]);
+        if (ok) tc_commit<PAIR>(&ctl->tmem_full[acc]);
       }
       // Drain: all tensor-core work this thread issued has completed.
-      tc_commit(&ctl->drain);
+      tc_commit_self<PAIR>(&ctl->drain);
       int drain_abort = 0;
       mbar_wait(&ctl->drain, 0, &drain_abort, p.err);
     }
@@ -341,31 +478,36 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1u;
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&ctl->tmem_full[acc], acc_phase, &ctl->abort, p.err);
+      if (lane == 0) ok = mbar_wait<PAIR>(&ctl->tmem_full[acc], acc_phase, &ctl->abort, p.err);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
       int m0, n0;
       tile_origin(p, m_units, CL, rank, tile, m0, n0);
-      const int row = m0 + quarter * 32 + lane;
-      __nv_bfloat16* yrow = p.y + static_cast<int64_t>(row) * p.n;
+      // after the quad transpose this lane stores piece (lane % 4) of rows
+      // row4 + 0..3: each store instruction covers 8 rows x 64 contiguous bytes
+      const int row4 = m0 + quarter * 32 + (lane & ~3);
       const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
       for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
         uint32_t r[32];
-        tmem_ld_32cols(taddr + c * 32, r);
+        tmem_ld_32cols(taddr + c * 32, r);          // this lane's row, columns col0 .. +31
         const int col0 = n0 + c * 32;
+        uint4 pc[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int col = col0 + g * 8;
-          if (col >= p.n) break;                          // N % 16 == 0: whole 8-column groups
+          const bool in = col < p.n;                      // N % 16 == 0: whole 8-column groups
           float v[8];
           float bz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (p.bias) bf16x8_to_f32(ld_cached(p.bias + col), bz);
+          if (p.bias && in) bf16x8_to_f32(ld_cached(p.bias + col), bz);
           float sc[8];
           if (FP8) {                                      // descales: activation x weight row
-            const float4 s0 = *reinterpret_cast<const float4*>(p.w_scale + col);
-            const float4 s1 = *reinterpret_cast<const float4*>(p.w_scale + col + 4);
+            float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+            if (in) {
+              s0 = *reinterpret_cast<const float4*>(p.w_scale + col);
+              s1 = *reinterpret_cast<const float4*>(p.w_scale + col + 4);
+            }
             const float ws[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) sc[e] = p.x_scale * ws[e];
@@ -376,22 +518,58 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
             const float a = FP8 ? fmaf(acc, sc[e], bz[e]) : acc + bz[e];
             v[e] = fast_act(a, p.act);
           }
-          if (row < p.m) st_16(yrow + col, f32x8_to_bf16x8(v));
+          pc[g] = f32x8_to_bf16x8(v);
+        }
+        quad_transpose(pc, lane & 3);
+        const int col = col0 + (lane & 3) * 8;
+        if (col < p.n) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (row4 + k < p.m) st_16(p.y + static_cast<int64_t>(row4 + k) * p.n + col, pc[k]);
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->tmem_empty[acc]);
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(map_cluster(smem_u32(&ctl->tmem_empty[acc]), 0));
+        else
+          mbar_arrive(&ctl->tmem_empty[acc]);
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();              // no multicast or remote arrive is left in flight to this CTA
+  if (PAIR) cluster_sync();                // the odd CTA's issue counts are in place
+  if (warp == 0 && lane == 0) {
+    // Every copy issued to this CTA (or, in a pair, to either CTA) has landed
+    // before the CTAs may exit: wait for the last phase of each stage
+    // (bounded; immediate on the normal path, where the MMAs consumed them all).
+    int drain_abort = 0;                   // own flag: the CTA one may already be set
+    if (!PAIR) {
+      for (int s = 0; s < S; ++s)
+        if (issued[s]) mbar_wait(&ctl->full[s], (issued[s] - 1) & 1u, &drain_abort, nullptr);
+    } else if (leader) {
+      for (int s = 0; s < S; ++s) {
+        const uint32_t mine = issued[s], theirs = ctl->peer_issued[s];
+        // After an abort the two producers may stand one k-block apart on a
+        // stage (each waits for the MMAs of the one before); complete the
+        // phase that only one of them filled.
+        if (theirs > mine)
+          mbar_arrive_expect_tx(&ctl->full[s], R::kStageBytes);   // the odd CTA's copies alone
+        else if (mine > theirs)
+          mbar_complete_tx(&ctl->full[s], R::kStageBytes);        // this CTA's copies alone
+        const uint32_t last = mine > theirs ? mine : theirs;
+        if (last) mbar_wait(&ctl->full[s], (last - 1) & 1u, &drain_abort, nullptr);
+      }
+    }
+  }
+  __syncthreads();
+  if (PAIR) cluster_sync();                // no copy, commit or remote arrive is left in flight to either CTA
   if (warp == 2) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
-                 : "memory");
+    tmem_dealloc<PAIR>(tmem_base);
   }
 }
 
@@ -432,21 +610,21 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8, int CL>
+template <bool FP8, bool PAIR>
 cudaError_t launch_gemm(const CUtensorMap& map_x, const CUtensorMap& map_w, const GemmParams& p, int sms,
                         cudaStream_t stream, const char** why) {
-  auto kern = linear_bias_gelu_kernel<FP8, CL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+  auto kern = linear_bias_gelu_kernel<FP8, PAIR>;
+  constexpr int CL = PAIR ? 2 : 1;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes<PAIR>()));
   if (e != cudaSuccess) {
     *why = "could not reserve shared memory";
     return e;
   }
   const int units = ((p.m_tiles + CL - 1) / CL) * p.n_tiles;
-  const int slots = sms / CL;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((units < slots ? units : slots) * CL));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes<PAIR>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -455,6 +633,18 @@ cudaError_t launch_gemm(const CUtensorMap& map_x, const CUtensorMap& map_w, cons
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // Persistent: as many clusters as can be resident at once (a GPC with an
+  // odd SM count leaves one SM out of the pairs), so no cluster waits for a
+  // second wave.
+  int slots = sms / CL;
+  if (PAIR) {
+    cfg.gridDim = dim3(static_cast<unsigned>(slots * CL));
+    int resident = 0;
+    if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) == cudaSuccess && resident > 0 && resident < slots)
+      slots = resident;
+    cudaGetLastError();
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>((units < slots ? units : slots) * CL));
   return cudaLaunchKernelEx(&cfg, kern, map_x, map_w, p);
 }
 
@@ -463,9 +653,9 @@ cudaError_t launch_gemm(const CUtensorMap& map_x, const CUtensorMap& map_w, cons
 cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, const char** why) {
   const bool fp8 = a.fp8 != 0;
   const int m_tiles = static_cast<int>((a.m + BM - 1) / BM);
-  const int cl = m_tiles >= 2 ? 2 : 1;                  // two-CTA clusters share W tiles
+  const bool pair = m_tiles >= 2;                        // CTA pairs on adjacent M tiles
   CUtensorMap map_x, map_w;
-  if (!make_map(&map_x, a.x, a.m, a.k, BM, fp8) || !make_map(&map_w, a.w, a.n, a.k, BN / cl, fp8)) {
+  if (!make_map(&map_x, a.x, a.m, a.k, BM, fp8) || !make_map(&map_w, a.w, a.n, a.k, pair ? BN / 2 : BN, fp8)) {
     *why = "cuTensorMapEncodeTiled is unavailable or rejected the operands";
     return cudaErrorInvalidValue;
   }
@@ -486,11 +676,11 @@ cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, cons
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaError_t e;
   if (fp8)
-    e = cl == 2 ? launch_gemm<true, 2>(map_x, map_w, p, sms, stream, why)
-                : launch_gemm<true, 1>(map_x, map_w, p, sms, stream, why);
+    e = pair ? launch_gemm<true, true>(map_x, map_w, p, sms, stream, why)
+             : launch_gemm<true, false>(map_x, map_w, p, sms, stream, why);
   else
-    e = cl == 2 ? launch_gemm<false, 2>(map_x, map_w, p, sms, stream, why)
-                : launch_gemm<false, 1>(map_x, map_w, p, sms, stream, why);
+    e = pair ? launch_gemm<false, true>(map_x, map_w, p, sms, stream, why)
+             : launch_gemm<false, false>(map_x, map_w, p, sms, stream, why);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

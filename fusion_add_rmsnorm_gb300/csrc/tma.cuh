@@ -52,15 +52,27 @@ GBF_DEVICE void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// CLUSTER: acquire at cluster scope, for a barrier that threads of another
+// CTA of the cluster arrive on (their arrive releases at cluster scope).
+template <bool CLUSTER = false>
 GBF_DEVICE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
+  if (CLUSTER)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
@@ -69,15 +81,20 @@ GBF_DEVICE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // so the wait ends even if the timer were to stall), or as soon as *abort is
 // set by another thread;
 // a thread that gives up on its own sets *abort and the device error bit.
+// SLEEP = false: no back-off between polls, for the lone thread of a pipeline
+// stage whose wake-up latency is on the critical path (mbarrier.try_wait
+// itself suspends the thread until the phase completes or a hardware time
+// limit passes, so the loop issues few instructions).
+template <bool CLUSTER = false, bool SLEEP = true>
 GBF_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, int* abort, unsigned int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = global_timer();
   uint32_t sleep_ns = 32;
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     // back off so a waiting thread does not flood the issue slots of the
     // threads doing the work (at most ~0.25 us of extra wake-up latency)
-    if (i > 4) {
+    if (SLEEP && i > 4) {
       __nanosleep(sleep_ns);
       if (sleep_ns < 256) sleep_ns <<= 1;
     }

@@ -250,7 +250,8 @@ GBF_API int gbf_copy(const void* src, void* dst, int64_t bytes, void* stream);
 /*
  * gbf_device_status -- synchronise `stream`, then read and clear the current
  * device's error word.  Returns GBF_OK, GBF_ETIMEOUT (a bounded wait gave up)
- * or GBF_EDEVICE (a cache slot was out of range), or GBF_ELAUNCH if the
+ * or GBF_EDEVICE (a cache slot was out of range, or the two CTAs of a GEMM
+ * tensor-core pair were given different TMEM bases), or GBF_ELAUNCH if the
  * synchronisation itself reported a CUDA error.
  */
 GBF_API int gbf_device_status(void* stream);
