@@ -207,9 +207,14 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
               oh[i] = f32x2_to_bf16x2(rh.x, rh.y);
             }
           } else {
-            // LayerNorm, two passes over the registers: mean, then centred
-            // squares; u = (x - mean) * inv * w + b, o = rotate(u).  The sums
-            // and the centring use the bf16-input FMA (x * 1 + acc, x * 1 - mean).
+            // LayerNorm: each lane takes the mean and the centred sum of
+            // squares of its own 16 values (two passes over registers), and
+            // the head's LPH lanes merge them in one shuffle chain by the
+            // pairwise update of Chan, Golub and LeVeque ("Algorithms for
+            // computing the sample variance", 1983) for equal counts:
+            // mean = (ma + mb) / 2, M2 = M2a + M2b + (mb - ma)^2 n / 2.
+            // Then u = (x - mean) * inv * w + b, o = rotate(u).  The sums and
+            // the centring use the bf16-input FMA (x * 1 + acc, x * 1 - mean).
             constexpr uint32_t kOnes = 0x3F803F80u;     // bf16x2 (1, 1)
             float m0 = 0.f, m1 = 0.f;
 #pragma unroll
@@ -219,9 +224,7 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
               m0 = fma_bf16_lo(xh[i], kOnes, m0);
               m1 = fma_bf16_hi(xh[i], kOnes, m1);
             }
-            const float mean = segment_sum(m0 + m1, LPH) * (1.0f / static_cast<float>(D));
-            // centred values are formed again in the output pass (one FMA each)
-            // rather than held in registers across it
+            float mean = (m0 + m1) * (1.0f / 16.0f);
             float v0 = 0.f, v1 = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -230,7 +233,24 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
               v0 = fmaf(c0, c0, fmaf(c2h, c2h, v0));
               v1 = fmaf(c1, c1, fmaf(c3, c3, v1));
             }
-            const float var = segment_sum(v0 + v1, LPH) * (1.0f / static_cast<float>(D));
+            float m2 = v0 + v1;
+            {
+              const unsigned seg = LPH >= 32 ? 0xffffffffu
+                                             : (((1u << LPH) - 1u) << ((threadIdx.x & 31u) & ~static_cast<unsigned>(LPH - 1)));
+              float half_n = 8.0f;                      // n / 2 for the n = 16 values of one lane
+#pragma unroll
+              for (int o = 1; o < LPH; o <<= 1) {
+                const float mo = __shfl_xor_sync(seg, mean, o);
+                const float m2o = __shfl_xor_sync(seg, m2, o);
+                const float d = mo - mean;
+                m2 = (m2 + m2o) + d * d * half_n;     // the same on both lanes of the exchange
+                mean = 0.5f * (mean + mo);
+                half_n *= 2.0f;
+              }
+            }
+            // centred values are formed again in the output pass (one FMA each)
+            // rather than held in registers across it
+            const float var = m2 * (1.0f / static_cast<float>(D));
             const bool is_q = h < a.n_q;
             if (!is_q && !slot_ok) continue;
             const float inv = rsqrtf(var + a.eps);
