@@ -84,206 +84,223 @@ GBF_DEVICE int64_t cache_slot(const QkvArgs& a, int64_t t, bool& ok) {
 
 // --------------------------------------------------------- per-head, 1D
 
-// Head groups per token: a template parameter G of the per-head kernel,
+// Head groups per token: a template parameter G of the per-head kernels,
 // chosen at launch so a thread has at most kRotBatch heads (one batch of
 // loads) where the token's 256 threads allow it.
 constexpr int kRotBlock = 256;
 constexpr int kRotBatch = 3;                // heads whose loads are in flight together
 
+// Loads of one batch of a thread's heads, h0, h0 + G, h0 + 2G, of a token row.
+template <int LPH, int G>
+GBF_DEVICE void rot1d_load(const __nv_bfloat16* row, int h0, int heads, int lane, uint4 (&lo)[kRotBatch],
+                           uint4 (&hi)[kRotBatch]) {
+  constexpr int D = LPH * 16;
+#pragma unroll
+  for (int u = 0; u < kRotBatch; ++u) {
+    const int h = h0 + u * G;
+    if (h < heads) {
+      lo[u] = ld_stream(row + h * D + lane * 8);
+      hi[u] = ld_stream(row + h * D + (lane + LPH) * 8);
+    }
+  }
+}
+
+// (cos, sin) table of a CTA's tokens: float4 [tok][i][lane] holds (cos, sin)
+// of slots 8 lane + 2i and 8 lane + 2i + 1, so the LPH lanes of a head read
+// consecutive float4s.
+template <int LPH>
+GBF_DEVICE void rot1d_cs_put(float4* cs4, int tc, int p, float2 cs) {
+  float* dst = reinterpret_cast<float*>(&cs4[(tc * 4 + ((p & 7) >> 1)) * LPH + (p >> 3)]) + 2 * (p & 1);
+  dst[0] = cs.x;
+  dst[1] = cs.y;
+}
+
+// Norm, rotation and stores of one batch of token t's heads (V heads are
+// copied); c2/s2 are the (cos, sin) of this lane's slots 8 lane .. 8 lane + 7
+// as pairs (2i, 2i + 1).
+template <int LPH, bool LN, int G>
+GBF_DEVICE void rot1d_batch(const QkvArgs& a, int64_t t, int h0, int lane, bool slot_ok, int64_t crow,
+                            const uint4 (&lo)[kRotBatch], const uint4 (&hi)[kRotBatch], const float2 (&c2)[4],
+                            const float2 (&s2)[4]) {
+  constexpr int D = LPH * 16;
+  const int heads = a.n_q + 2 * a.n_kv;
+  // last head of the batch first: V heads come last in the row, and copying
+  // them out first frees their registers for the norm work
+#pragma unroll
+  for (int uu = 0; uu < kRotBatch; ++uu) {
+    const int u = kRotBatch - 1 - uu;
+    const int h = h0 + u * G;
+    if (h >= heads) continue;
+    if (h >= a.n_q + a.n_kv) {               // V: pass through
+      if (slot_ok) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.v_cache) +
+                             (crow * a.n_kv + (h - a.n_q - a.n_kv)) * D;
+        st_16(dst + lane * 8, lo[u]);
+        st_16(dst + (lane + LPH) * 8, hi[u]);
+      }
+      continue;
+    }
+    const uint32_t xl[4] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w};
+    const uint32_t xh[4] = {hi[u].x, hi[u].y, hi[u].z, hi[u].w};
+    uint32_t ol[4], oh[4];
+    if (!LN) {
+      // RMSNorm: o = rotate(x * w) * inv
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s0 = fma_bf16_lo(xl[i], xl[i], s0);
+        s1 = fma_bf16_hi(xl[i], xl[i], s1);
+        s0 = fma_bf16_lo(xh[i], xh[i], s0);
+        s1 = fma_bf16_hi(xh[i], xh[i], s1);
+      }
+      const float ss = segment_sum(s0 + s1, LPH);   // the head's LPH lanes only
+      const bool is_q = h < a.n_q;
+      if (!is_q && !slot_ok) continue;
+      const float inv = rsqrtf(ss / static_cast<float>(D) + a.eps);
+      const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(is_q ? a.q_w : a.k_w);
+      const uint4 wlv = ld_cached(w + lane * 8), whv = ld_cached(w + (lane + LPH) * 8);
+      const uint32_t wl[4] = {wlv.x, wlv.y, wlv.z, wlv.w};
+      const uint32_t wh[4] = {whv.x, whv.y, whv.z, whv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        // pair (8 lane + 2i + j, the same + D/2) for j = 0, 1 in the two float2 lanes
+        const float2 ul = make_float2(fma_bf16_lo(xl[i], wl[i], 0.f), fma_bf16_hi(xl[i], wl[i], 0.f));
+        const float2 uh = make_float2(fma_bf16_lo(xh[i], wh[i], 0.f), fma_bf16_hi(xh[i], wh[i], 0.f));
+        float2 rl, rh;
+        rl.x = fmaf(ul.x, c2[i].x, -(s2[i].x * uh.x)) * inv;
+        rl.y = fmaf(ul.y, c2[i].y, -(s2[i].y * uh.y)) * inv;
+        rh.x = fmaf(uh.x, c2[i].x, s2[i].x * ul.x) * inv;
+        rh.y = fmaf(uh.y, c2[i].y, s2[i].y * ul.y) * inv;
+        ol[i] = f32x2_to_bf16x2(rl.x, rl.y);
+        oh[i] = f32x2_to_bf16x2(rh.x, rh.y);
+      }
+    } else {
+      // LayerNorm: each lane takes the mean and the centred sum of
+      // squares of its own 16 values (two passes over registers), and
+      // the head's LPH lanes merge them in one shuffle chain by the
+      // pairwise update of Chan, Golub and LeVeque ("Algorithms for
+      // computing the sample variance", 1983) for equal counts:
+      // mean = (ma + mb) / 2, M2 = M2a + M2b + (mb - ma)^2 n / 2.
+      // Then u = (x - mean) * inv * w + b, o = rotate(u).  The sums and
+      // the centring use the bf16-input FMA (x * 1 + acc, x * 1 - mean).
+      constexpr uint32_t kOnes = 0x3F803F80u;     // bf16x2 (1, 1)
+      float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        m0 = fma_bf16_lo(xl[i], kOnes, m0);
+        m1 = fma_bf16_hi(xl[i], kOnes, m1);
+        m0 = fma_bf16_lo(xh[i], kOnes, m0);
+        m1 = fma_bf16_hi(xh[i], kOnes, m1);
+      }
+      float mean = (m0 + m1) * (1.0f / 16.0f);
+      float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float c0 = fma_bf16_lo(xl[i], kOnes, -mean), c1 = fma_bf16_hi(xl[i], kOnes, -mean);
+        const float c2h = fma_bf16_lo(xh[i], kOnes, -mean), c3 = fma_bf16_hi(xh[i], kOnes, -mean);
+        v0 = fmaf(c0, c0, fmaf(c2h, c2h, v0));
+        v1 = fmaf(c1, c1, fmaf(c3, c3, v1));
+      }
+      float m2 = v0 + v1;
+      {
+        const unsigned seg = LPH >= 32 ? 0xffffffffu
+                                       : (((1u << LPH) - 1u) << ((threadIdx.x & 31u) & ~static_cast<unsigned>(LPH - 1)));
+        float half_n = 8.0f;                      // n / 2 for the n = 16 values of one lane
+#pragma unroll
+        for (int o = 1; o < LPH; o <<= 1) {
+          const float mo = __shfl_xor_sync(seg, mean, o);
+          const float m2o = __shfl_xor_sync(seg, m2, o);
+          const float d = mo - mean;
+          m2 = (m2 + m2o) + d * d * half_n;     // the same on both lanes of the exchange
+          mean = 0.5f * (mean + mo);
+          half_n *= 2.0f;
+        }
+      }
+      // centred values are formed again in the output pass (one FMA each)
+      // rather than held in registers across it
+      const float var = m2 * (1.0f / static_cast<float>(D));
+      const bool is_q = h < a.n_q;
+      if (!is_q && !slot_ok) continue;
+      const float inv = rsqrtf(var + a.eps);
+      const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(is_q ? a.q_w : a.k_w);
+      const __nv_bfloat16* bb = static_cast<const __nv_bfloat16*>(is_q ? a.q_b : a.k_b);
+      const uint4 wlv = ld_cached(w + lane * 8), whv = ld_cached(w + (lane + LPH) * 8);
+      const uint4 blv = bb ? ld_cached(bb + lane * 8) : make_uint4(0, 0, 0, 0);
+      const uint4 bhv = bb ? ld_cached(bb + (lane + LPH) * 8) : make_uint4(0, 0, 0, 0);
+      const uint32_t wl[4] = {wlv.x, wlv.y, wlv.z, wlv.w}, wh[4] = {whv.x, whv.y, whv.z, whv.w};
+      const uint32_t bl[4] = {blv.x, blv.y, blv.z, blv.w}, bh[4] = {bhv.x, bhv.y, bhv.z, bhv.w};
+      // (lo, hi) halves of a packed bf16 pair as two floats
+      auto pair = [](uint32_t v) { return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u)); };
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 inv2 = make_float2(inv, inv);
+        const float2 cl2 = make_float2(fma_bf16_lo(xl[i], kOnes, -mean), fma_bf16_hi(xl[i], kOnes, -mean));
+        const float2 ch2 = make_float2(fma_bf16_lo(xh[i], kOnes, -mean), fma_bf16_hi(xh[i], kOnes, -mean));
+        const float2 ul = __ffma2_rn(__fmul2_rn(cl2, inv2), pair(wl[i]), pair(bl[i]));
+        const float2 uh = __ffma2_rn(__fmul2_rn(ch2, inv2), pair(wh[i]), pair(bh[i]));
+        const float2 rl = __ffma2_rn(ul, c2[i], __fmul2_rn(make_float2(-s2[i].x, -s2[i].y), uh));
+        const float2 rh = __ffma2_rn(uh, c2[i], __fmul2_rn(s2[i], ul));
+        ol[i] = f32x2_to_bf16x2(rl.x, rl.y);
+        oh[i] = f32x2_to_bf16x2(rh.x, rh.y);
+      }
+    }
+    const bool is_q = h < a.n_q;
+    __nv_bfloat16* dst = is_q ? static_cast<__nv_bfloat16*>(a.q_out) + (t * a.n_q + h) * D
+                              : static_cast<__nv_bfloat16*>(a.k_cache) + (crow * a.n_kv + (h - a.n_q)) * D;
+    st_16(dst + lane * 8, make_uint4(ol[0], ol[1], ol[2], ol[3]));
+    st_16(dst + (lane + LPH) * 8, make_uint4(oh[0], oh[1], oh[2], oh[3]));
+  }
+}
+
+template <int LPH>
+GBF_DEVICE void rot1d_cs_read(const float4* cs_tok, int lane, float2 (&c2)[4], float2 (&s2)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 q = cs_tok[i * LPH + lane];
+    c2[i] = make_float2(q.x, q.z);
+    s2[i] = make_float2(q.y, q.w);
+  }
+}
+
+// One CTA per TOK tokens; a thread with more than one batch of heads takes
+// them in turn.  The first batch is requested before the (cos, sin) table.
 template <int LPH, bool LN, int G>
 __global__ void __launch_bounds__(kRotBlock, LN ? 3 : 4)
 qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
-  constexpr int kRotGroups = G;
   constexpr int D = LPH * 16;
   constexpr int SLOTS = D / 2;
-  constexpr int TPT = kRotGroups * LPH;     // threads per token
-  constexpr int TOK = kRotBlock / TPT;      // tokens per CTA pass
+  constexpr int TPT = G * LPH;              // threads per token
+  constexpr int TOK = kRotBlock / TPT;      // tokens per CTA
   static_assert(TOK * SLOTS <= kRotBlock, "at most one (cos, sin) per thread");
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x % LPH;
-  const int grp = (threadIdx.x / LPH) % kRotGroups;
+  const int grp = (threadIdx.x / LPH) % G;
   const int tok = threadIdx.x / TPT;
   const int heads = a.n_q + 2 * a.n_kv;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * TOK + tok;
   const bool live = t < a.tokens;
   const __nv_bfloat16* row = static_cast<const __nv_bfloat16*>(a.qkv) + t * static_cast<int64_t>(heads) * D;
-  // Heads grp, grp + kRotGroups, ... in batches whose loads are all issued
-  // first; the first batch is requested before the (cos, sin) table is built.
   uint4 lo[kRotBatch], hi[kRotBatch];
-  auto load_batch = [&](int h0) {
-#pragma unroll
-    for (int u = 0; u < kRotBatch; ++u) {
-      const int h = h0 + u * kRotGroups;
-      if (h < heads) {
-        lo[u] = ld_stream(row + h * D + lane * 8);
-        hi[u] = ld_stream(row + h * D + (lane + LPH) * 8);
-      }
-    }
-  };
-  if (live) load_batch(grp);
+  if (live) rot1d_load<LPH, G>(row, grp, heads, lane, lo, hi);
 
-  // (cos, sin) of the CTA's tokens: float4 [tok][i][lane] holds (cos, sin) of
-  // slots 8 lane + 2i and 8 lane + 2i + 1, so the LPH lanes of a head read
-  // consecutive float4s.  Thread (tc, p) computes slot p of token tc.
   __shared__ float4 cs4[TOK * 4 * LPH];
   {
-    const int tc = threadIdx.x / SLOTS, p = threadIdx.x % SLOTS;
+    const int tc = threadIdx.x / SLOTS, p = threadIdx.x % SLOTS;      // slot p of token tc
     const int64_t tcs = static_cast<int64_t>(blockIdx.x) * TOK + tc;
-    if (tc < TOK && tcs < a.tokens) {
-      const float2 cs = rope_cos_sin(a.pos[tcs], a.omega_hi[p], a.omega_lo[p]);
-      float* dst = reinterpret_cast<float*>(&cs4[(tc * 4 + ((p & 7) >> 1)) * LPH + (p >> 3)]) + 2 * (p & 1);
-      dst[0] = cs.x;
-      dst[1] = cs.y;
-    }
+    if (tc < TOK && tcs < a.tokens) rot1d_cs_put<LPH>(cs4, tc, p, rope_cos_sin(a.pos[tcs], a.omega_hi[p], a.omega_lo[p]));
   }
   __syncthreads();
-
-  {
-    if (live) {
-      bool slot_ok;
-      const int64_t crow = cache_slot(a, t, slot_ok);
-      if (!slot_ok && threadIdx.x % TPT == 0) raise_error(a.err, DEV_ERR_SLOT_RANGE);
-      // (cos, sin) of this lane's slots 8*lane .. 8*lane + 7, as pairs (2i, 2i + 1)
-      float2 c2[4], s2[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 q = cs4[(tok * 4 + i) * LPH + lane];
-        c2[i] = make_float2(q.x, q.z);
-        s2[i] = make_float2(q.y, q.w);
-      }
-
-      // The trip count depends only on grp, which all LPH lanes of a head share.
-      for (int h0 = grp; h0 < heads; h0 += kRotBatch * kRotGroups) {
-        if (h0 != grp) load_batch(h0);
-#pragma unroll
-        // last head of the batch first: V heads come last in the row, and
-        // copying them out first frees their registers for the norm work
-        for (int uu = 0; uu < kRotBatch; ++uu) {
-          const int u = kRotBatch - 1 - uu;
-          const int h = h0 + u * kRotGroups;
-          if (h >= heads) continue;
-          if (h >= a.n_q + a.n_kv) {               // V: pass through
-            if (slot_ok) {
-              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.v_cache) +
-                                   (crow * a.n_kv + (h - a.n_q - a.n_kv)) * D;
-              st_16(dst + lane * 8, lo[u]);
-              st_16(dst + (lane + LPH) * 8, hi[u]);
-            }
-            continue;
-          }
-          const uint32_t xl[4] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w};
-          const uint32_t xh[4] = {hi[u].x, hi[u].y, hi[u].z, hi[u].w};
-          uint32_t ol[4], oh[4];
-          if (!LN) {
-            // RMSNorm: o = rotate(x * w) * inv
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              s0 = fma_bf16_lo(xl[i], xl[i], s0);
-              s1 = fma_bf16_hi(xl[i], xl[i], s1);
-              s0 = fma_bf16_lo(xh[i], xh[i], s0);
-              s1 = fma_bf16_hi(xh[i], xh[i], s1);
-            }
-            const float ss = segment_sum(s0 + s1, LPH);   // the head's LPH lanes only
-            const bool is_q = h < a.n_q;
-            if (!is_q && !slot_ok) continue;
-            const float inv = rsqrtf(ss / static_cast<float>(D) + a.eps);
-            const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(is_q ? a.q_w : a.k_w);
-            const uint4 wlv = ld_cached(w + lane * 8), whv = ld_cached(w + (lane + LPH) * 8);
-            const uint32_t wl[4] = {wlv.x, wlv.y, wlv.z, wlv.w};
-            const uint32_t wh[4] = {whv.x, whv.y, whv.z, whv.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              // pair (8 lane + 2i + j, the same + D/2) for j = 0, 1 in the two float2 lanes
-              const float2 ul = make_float2(fma_bf16_lo(xl[i], wl[i], 0.f), fma_bf16_hi(xl[i], wl[i], 0.f));
-              const float2 uh = make_float2(fma_bf16_lo(xh[i], wh[i], 0.f), fma_bf16_hi(xh[i], wh[i], 0.f));
-              float2 rl, rh;
-              rl.x = fmaf(ul.x, c2[i].x, -(s2[i].x * uh.x)) * inv;
-              rl.y = fmaf(ul.y, c2[i].y, -(s2[i].y * uh.y)) * inv;
-              rh.x = fmaf(uh.x, c2[i].x, s2[i].x * ul.x) * inv;
-              rh.y = fmaf(uh.y, c2[i].y, s2[i].y * ul.y) * inv;
-              ol[i] = f32x2_to_bf16x2(rl.x, rl.y);
-              oh[i] = f32x2_to_bf16x2(rh.x, rh.y);
-            }
-          } else {
-            // LayerNorm: each lane takes the mean and the centred sum of
-            // squares of its own 16 values (two passes over registers), and
-            // the head's LPH lanes merge them in one shuffle chain by the
-            // pairwise update of Chan, Golub and LeVeque ("Algorithms for
-            // computing the sample variance", 1983) for equal counts:
-            // mean = (ma + mb) / 2, M2 = M2a + M2b + (mb - ma)^2 n / 2.
-            // Then u = (x - mean) * inv * w + b, o = rotate(u).  The sums and
-            // the centring use the bf16-input FMA (x * 1 + acc, x * 1 - mean).
-            constexpr uint32_t kOnes = 0x3F803F80u;     // bf16x2 (1, 1)
-            float m0 = 0.f, m1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              m0 = fma_bf16_lo(xl[i], kOnes, m0);
-              m1 = fma_bf16_hi(xl[i], kOnes, m1);
-              m0 = fma_bf16_lo(xh[i], kOnes, m0);
-              m1 = fma_bf16_hi(xh[i], kOnes, m1);
-            }
-            float mean = (m0 + m1) * (1.0f / 16.0f);
-            float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float c0 = fma_bf16_lo(xl[i], kOnes, -mean), c1 = fma_bf16_hi(xl[i], kOnes, -mean);
-              const float c2h = fma_bf16_lo(xh[i], kOnes, -mean), c3 = fma_bf16_hi(xh[i], kOnes, -mean);
-              v0 = fmaf(c0, c0, fmaf(c2h, c2h, v0));
-              v1 = fmaf(c1, c1, fmaf(c3, c3, v1));
-            }
-            float m2 = v0 + v1;
-            {
-              const unsigned seg = LPH >= 32 ? 0xffffffffu
-                                             : (((1u << LPH) - 1u) << ((threadIdx.x & 31u) & ~static_cast<unsigned>(LPH - 1)));
-              float half_n = 8.0f;                      // n / 2 for the n = 16 values of one lane
-#pragma unroll
-              for (int o = 1; o < LPH; o <<= 1) {
-                const float mo = __shfl_xor_sync(seg, mean, o);
-                const float m2o = __shfl_xor_sync(seg, m2, o);
-                const float d = mo - mean;
-                m2 = (m2 + m2o) + d * d * half_n;     // the same on both lanes of the exchange
-                mean = 0.5f * (mean + mo);
-                half_n *= 2.0f;
-              }
-            }
-            // centred values are formed again in the output pass (one FMA each)
-            // rather than held in registers across it
-            const float var = m2 * (1.0f / static_cast<float>(D));
-            const bool is_q = h < a.n_q;
-            if (!is_q && !slot_ok) continue;
-            const float inv = rsqrtf(var + a.eps);
-            const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(is_q ? a.q_w : a.k_w);
-            const __nv_bfloat16* bb = static_cast<const __nv_bfloat16*>(is_q ? a.q_b : a.k_b);
-            const uint4 wlv = ld_cached(w + lane * 8), whv = ld_cached(w + (lane + LPH) * 8);
-            const uint4 blv = bb ? ld_cached(bb + lane * 8) : make_uint4(0, 0, 0, 0);
-            const uint4 bhv = bb ? ld_cached(bb + (lane + LPH) * 8) : make_uint4(0, 0, 0, 0);
-            const uint32_t wl[4] = {wlv.x, wlv.y, wlv.z, wlv.w}, wh[4] = {whv.x, whv.y, whv.z, whv.w};
-            const uint32_t bl[4] = {blv.x, blv.y, blv.z, blv.w}, bh[4] = {bhv.x, bhv.y, bhv.z, bhv.w};
-            // (lo, hi) halves of a packed bf16 pair as two floats
-            auto pair = [](uint32_t v) { return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u)); };
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 inv2 = make_float2(inv, inv);
-              const float2 cl2 = make_float2(fma_bf16_lo(xl[i], kOnes, -mean), fma_bf16_hi(xl[i], kOnes, -mean));
-              const float2 ch2 = make_float2(fma_bf16_lo(xh[i], kOnes, -mean), fma_bf16_hi(xh[i], kOnes, -mean));
-              const float2 ul = __ffma2_rn(__fmul2_rn(cl2, inv2), pair(wl[i]), pair(bl[i]));
-              const float2 uh = __ffma2_rn(__fmul2_rn(ch2, inv2), pair(wh[i]), pair(bh[i]));
-              const float2 rl = __ffma2_rn(ul, c2[i], __fmul2_rn(make_float2(-s2[i].x, -s2[i].y), uh));
-              const float2 rh = __ffma2_rn(uh, c2[i], __fmul2_rn(s2[i], ul));
-              ol[i] = f32x2_to_bf16x2(rl.x, rl.y);
-              oh[i] = f32x2_to_bf16x2(rh.x, rh.y);
-            }
-          }
-          const bool is_q = h < a.n_q;
-          __nv_bfloat16* dst = is_q ? static_cast<__nv_bfloat16*>(a.q_out) + (t * a.n_q + h) * D
-                                    : static_cast<__nv_bfloat16*>(a.k_cache) + (crow * a.n_kv + (h - a.n_q)) * D;
-          st_16(dst + lane * 8, make_uint4(ol[0], ol[1], ol[2], ol[3]));
-          st_16(dst + (lane + LPH) * 8, make_uint4(oh[0], oh[1], oh[2], oh[3]));
-        }
-      }
-    }
+  if (!live) return;
+  bool slot_ok;
+  const int64_t crow = cache_slot(a, t, slot_ok);
+  if (!slot_ok && threadIdx.x % TPT == 0) raise_error(a.err, DEV_ERR_SLOT_RANGE);
+  float2 c2[4], s2[4];
+  rot1d_cs_read<LPH>(cs4 + tok * 4 * LPH, lane, c2, s2);
+  // The trip count depends only on grp, which all LPH lanes of a head share.
+  for (int h0 = grp; h0 < heads; h0 += kRotBatch * G) {
+    if (h0 != grp) rot1d_load<LPH, G>(row, h0, heads, lane, lo, hi);
+    rot1d_batch<LPH, LN, G>(a, t, h0, lane, slot_ok, crow, lo, hi, c2, s2);
   }
 }
 
