@@ -34,9 +34,11 @@
 //   warps 4-11 epilogue (each CTA): tcgen05.ld 32 columns at a time (warp w
 //              reads TMEM lanes 32 (w % 4) .. +31, one output row per thread,
 //              half of the tile's columns), descales and bias, the activation
-//              (fast forms, see common.cuh), round to bf16; a 4 x 4 shuffle
-//              transpose inside each lane quad turns the one-row-per-lane
-//              layout into stores of 8 rows x 64 contiguous bytes;
+//              (fast forms, see common.cuh), round to bf16 into a 32-row x
+//              64-column box in shared memory (128-byte swizzle, so the
+//              one-row-per-lane writes are conflict-free), written out by
+//              one bulk tensor store (cp.async.bulk.tensor) that clips at M
+//              and N;
 //              then the warp arrives on the even CTA's "accumulator free"
 //              barrier.
 // Tile order: the N tiles are cut into groups of kGroupN; inside a group the
@@ -69,11 +71,17 @@ constexpr int kThreads = 384;
 constexpr int kEpilogueWarp0 = 4;                // warps 4..11: two per TMEM lane quarter
 constexpr int kEpilogueWarps = 8;
 
+// Output staging: each epilogue warp packs 32 rows x 64 columns of bf16 (one
+// 128-byte-swizzled TMA box) before a bulk tensor store.
+constexpr int kOutCols = 64;
+constexpr int kOutBoxBytes = 32 * kOutCols * 2;              // 4 KB
+constexpr int kOutBytes = kEpilogueWarps * kOutBoxBytes;      // 32 KB
+
 // Shared-memory ring of one CTA: unpaired, the whole W tile per stage; paired,
 // half of it (the other half sits in the other CTA).
 template <bool PAIR>
 struct Ring {
-  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kStages = PAIR ? 6 : 3;
   static constexpr int kBRows = PAIR ? BN / 2 : BN;
   static constexpr int kBStageBytes = kBRows * BK_BYTES;
   static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes;
@@ -93,7 +101,7 @@ struct __align__(8) SharedCtl {
 
 template <bool PAIR>
 constexpr size_t smem_bytes() {
-  return 1024 /* alignment slack */ + Ring<PAIR>::kStages * Ring<PAIR>::kStageBytes +
+  return 1024 /* alignment slack */ + Ring<PAIR>::kStages * Ring<PAIR>::kStageBytes + kOutBytes +
          sizeof(SharedCtl<Ring<PAIR>::kStages>);
 }
 
@@ -114,6 +122,14 @@ GBF_DEVICE void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar
       " [%0], [%1, {%3, %4}], [%2];"
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
+}
+
+// Bulk tensor store of the box at shared address `src` to coordinates
+// (c0, c1) of `map`; elements outside the tensor are not written.
+GBF_DEVICE void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
 }
 
 GBF_DEVICE uint32_t cluster_ctarank() {
@@ -259,33 +275,6 @@ GBF_DEVICE void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-GBF_DEVICE uint4 shfl_xor_u4(uint4 v, int m) {
-  v.x = __shfl_xor_sync(0xffffffffu, v.x, m);
-  v.y = __shfl_xor_sync(0xffffffffu, v.y, m);
-  v.z = __shfl_xor_sync(0xffffffffu, v.z, m);
-  v.w = __shfl_xor_sync(0xffffffffu, v.w, m);
-  return v;
-}
-
-// 4 x 4 transpose of 16-byte pieces inside each group of four lanes: on entry
-// lane 4q + i holds pieces 0..3 of its own row; on exit it holds piece i of
-// rows 4q + 0..3.  Two exchange rounds: the off-diagonal 2 x 2 blocks with
-// lane ^ 2, then the off-diagonal pieces inside each block with lane ^ 1.
-GBF_DEVICE void quad_transpose(uint4 (&pc)[4], int i) {
-  const bool hi2 = (i & 2) != 0;
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const uint4 r = shfl_xor_u4(hi2 ? pc[j] : pc[j + 2], 2);
-    if (hi2) pc[j] = r; else pc[j + 2] = r;
-  }
-  const bool hi1 = (i & 1) != 0;
-#pragma unroll
-  for (int j = 0; j < 4; j += 2) {
-    const uint4 r = shfl_xor_u4(hi1 ? pc[j] : pc[j + 1], 1);
-    if (hi1) pc[j] = r; else pc[j + 1] = r;
-  }
-}
-
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the
 // 128-byte swizzle: rows of 128 bytes, 8-row core groups 1024 bytes apart
 // (stride byte offset), descriptor version 1, layout "swizzle 128B".
@@ -311,7 +300,6 @@ constexpr int kGroupN = 16;
 
 struct GemmParams {
   const __nv_bfloat16* bias;
-  __nv_bfloat16* y;
   const float* w_scale;      // E4M3 weights: descale per output channel
   float x_scale;             // E4M3 activations: the descale
   unsigned int* err;
@@ -337,7 +325,7 @@ GBF_DEVICE void tile_origin(const GemmParams& p, int m_units, int cl, int rank, 
 template <bool FP8, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
-                        const GemmParams p) {
+                        const __grid_constant__ CUtensorMap map_y, const GemmParams p) {
   using R = Ring<PAIR>;
   constexpr int S = R::kStages;
   constexpr int CL = PAIR ? 2 : 1;
@@ -349,7 +337,8 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smem_a = smem;                                   // S x 16 KB
   uint8_t* smem_b = smem + S * A_STAGE_BYTES;               // S x (32 or 16) KB
-  SharedCtl<S>* ctl = reinterpret_cast<SharedCtl<S>*>(smem + S * R::kStageBytes);
+  uint8_t* smem_out = smem + S * R::kStageBytes;            // 8 x 4 KB output boxes (1 KB aligned)
+  SharedCtl<S>* ctl = reinterpret_cast<SharedCtl<S>*>(smem_out + kOutBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -374,6 +363,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
     mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_y)) : "memory");
   }
   if (warp == 2) tmem_alloc<PAIR>(&ctl->tmem_base);
   tc_fence_before();
@@ -473,6 +463,8 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31 (warp % 4)
     const int half = (warp - kEpilogueWarp0) >> 2;      // columns 128*half .. +127 of the tile
+    uint8_t* my_out = smem_out + (warp - kEpilogueWarp0) * kOutBoxBytes;
+    const uint32_t out32 = smem_u32(my_out);
     int local = 0;
     for (int tile = first; tile < num_tiles; tile += stride, ++local) {
       const int acc = local & 1;
@@ -484,48 +476,56 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       tc_fence_after();
       int m0, n0;
       tile_origin(p, m_units, CL, rank, tile, m0, n0);
-      // after the quad transpose this lane stores piece (lane % 4) of rows
-      // row4 + 0..3: each store instruction covers 8 rows x 64 contiguous bytes
-      const int row4 = m0 + quarter * 32 + (lane & ~3);
+      const int row0 = m0 + quarter * 32;                 // this warp's 32 rows; lane = row within them
       const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
-        uint32_t r[32];
-        tmem_ld_32cols(taddr + c * 32, r);          // this lane's row, columns col0 .. +31
-        const int col0 = n0 + c * 32;
-        uint4 pc[4];
+      for (int box = 0; box < BN / 2 / kOutCols; ++box) {
+        const int cbase = half * (BN / 2) + box * kOutCols;   // tile column of the box
+        const int col0 = n0 + cbase;
+        // the previous box's store has finished reading the staging buffer
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll 1
+        for (int sub = 0; sub < kOutCols / 32; ++sub) {
+          uint32_t r[32];
+          tmem_ld_32cols(taddr + cbase + sub * 32, r);      // this lane's row, 32 columns
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int col = col0 + g * 8;
-          const bool in = col < p.n;                      // N % 16 == 0: whole 8-column groups
-          float v[8];
-          float bz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (p.bias && in) bf16x8_to_f32(ld_cached(p.bias + col), bz);
-          float sc[8];
-          if (FP8) {                                      // descales: activation x weight row
-            float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-            if (in) {
-              s0 = *reinterpret_cast<const float4*>(p.w_scale + col);
-              s1 = *reinterpret_cast<const float4*>(p.w_scale + col + 4);
+          for (int g = 0; g < 4; ++g) {
+            const int col = col0 + sub * 32 + g * 8;
+            const bool in = col < p.n;                      // N % 16 == 0: whole 8-column groups
+            float v[8];
+            float bz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (p.bias && in) bf16x8_to_f32(ld_cached(p.bias + col), bz);
+            float sc[8];
+            if (FP8) {                                      // descales: activation x weight row
+              float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+              if (in) {
+                s0 = *reinterpret_cast<const float4*>(p.w_scale + col);
+                s1 = *reinterpret_cast<const float4*>(p.w_scale + col + 4);
+              }
+              const float ws[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) sc[e] = p.x_scale * ws[e];
             }
-            const float ws[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sc[e] = p.x_scale * ws[e];
+            for (int e = 0; e < 8; ++e) {
+              const float acc = __uint_as_float(r[g * 8 + e]);
+              const float a = FP8 ? fmaf(acc, sc[e], bz[e]) : acc + bz[e];
+              v[e] = fast_act(a, p.act);
+            }
+            // 16-byte piece j of row `lane` sits at piece j ^ (row % 8) (the TMA 128-byte swizzle)
+            const int j = sub * 4 + g;
+            const uint4 pk = f32x8_to_bf16x8(v);
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(out32 + lane * 128 + ((j ^ (lane & 7)) << 4)),
+                         "r"(pk.x), "r"(pk.y), "r"(pk.z), "r"(pk.w)
+                         : "memory");
           }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float acc = __uint_as_float(r[g * 8 + e]);
-            const float a = FP8 ? fmaf(acc, sc[e], bz[e]) : acc + bz[e];
-            v[e] = fast_act(a, p.act);
-          }
-          pc[g] = f32x8_to_bf16x8(v);
         }
-        quad_transpose(pc, lane & 3);
-        const int col = col0 + (lane & 3) * 8;
-        if (col < p.n) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (row4 + k < p.m) st_16(p.y + static_cast<int64_t>(row4 + k) * p.n + col, pc[k]);
+        fence_proxy_async_smem();                         // the pieces are visible to the bulk store
+        __syncwarp();
+        if (lane == 0 && col0 < p.n && row0 < p.m) {
+          tma_store_2d(&map_y, my_out, col0, row0);
+          bulk_commit();
         }
       }
       tc_fence_before();
@@ -537,6 +537,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
           mbar_arrive(&ctl->tmem_empty[acc]);
       }
     }
+    if (lane == 0) bulk_wait_all();                       // every output store of this warp has completed
   }
 
   tc_fence_before();
@@ -595,7 +596,7 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2D tensor [rows, cols] (cols contiguous) of bf16 or of bytes (E4M3), box
-// [box_rows, 128 bytes of K], 128-byte swizzle.
+// [box_rows, 128 bytes of cols], 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, bool fp8) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -611,7 +612,8 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
 }
 
 template <bool FP8, bool PAIR>
-cudaError_t launch_gemm(const CUtensorMap& map_x, const CUtensorMap& map_w, const GemmParams& p, int sms,
+cudaError_t launch_gemm(const CUtensorMap& map_x, const CUtensorMap& map_w, const CUtensorMap& map_y,
+                        const GemmParams& p, int sms,
                         cudaStream_t stream, const char** why) {
   auto kern = linear_bias_gelu_kernel<FP8, PAIR>;
   constexpr int CL = PAIR ? 2 : 1;
@@ -645,7 +647,7 @@ cudaError_t launch_gemm(const CUtensorMap& map_x, const CUtensorMap& map_w, cons
     cudaGetLastError();
   }
   cfg.gridDim = dim3(static_cast<unsigned>((units < slots ? units : slots) * CL));
-  return cudaLaunchKernelEx(&cfg, kern, map_x, map_w, p);
+  return cudaLaunchKernelEx(&cfg, kern, map_x, map_w, map_y, p);
 }
 
 }  // namespace
@@ -654,14 +656,14 @@ cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, cons
   const bool fp8 = a.fp8 != 0;
   const int m_tiles = static_cast<int>((a.m + BM - 1) / BM);
   const bool pair = m_tiles >= 2;                        // CTA pairs on adjacent M tiles
-  CUtensorMap map_x, map_w;
-  if (!make_map(&map_x, a.x, a.m, a.k, BM, fp8) || !make_map(&map_w, a.w, a.n, a.k, pair ? BN / 2 : BN, fp8)) {
+  CUtensorMap map_x, map_w, map_y;
+  if (!make_map(&map_x, a.x, a.m, a.k, BM, fp8) || !make_map(&map_w, a.w, a.n, a.k, pair ? BN / 2 : BN, fp8) ||
+      !make_map(&map_y, a.y, a.m, a.n, 32, false)) {
     *why = "cuTensorMapEncodeTiled is unavailable or rejected the operands";
     return cudaErrorInvalidValue;
   }
   GemmParams p;
   p.bias = static_cast<const __nv_bfloat16*>(a.bias);
-  p.y = static_cast<__nv_bfloat16*>(a.y);
   p.w_scale = a.w_scale;
   p.x_scale = a.x_scale;
   p.err = a.err;
@@ -676,11 +678,11 @@ cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, cons
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaError_t e;
   if (fp8)
-    e = pair ? launch_gemm<true, true>(map_x, map_w, p, sms, stream, why)
-             : launch_gemm<true, false>(map_x, map_w, p, sms, stream, why);
+    e = pair ? launch_gemm<true, true>(map_x, map_w, map_y, p, sms, stream, why)
+             : launch_gemm<true, false>(map_x, map_w, map_y, p, sms, stream, why);
   else
-    e = pair ? launch_gemm<false, true>(map_x, map_w, p, sms, stream, why)
-             : launch_gemm<false, false>(map_x, map_w, p, sms, stream, why);
+    e = pair ? launch_gemm<false, true>(map_x, map_w, map_y, p, sms, stream, why)
+             : launch_gemm<false, false>(map_x, map_w, map_y, p, sms, stream, why);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
