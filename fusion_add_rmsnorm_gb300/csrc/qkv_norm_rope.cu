@@ -512,8 +512,17 @@ qkv_staged_kernel(const __grid_constant__ QkvArgs a) {
       cs_pos[cs_slot(my_slot.hi_axis & 0xFFFF, vph)] = cs;
     }
 
-    // Phase 1: x * w of Q/K to `u`, V from the ring buffer straight out.
+    // Phase 1: x * w of Q/K to `u`; V (contiguous in the row and in its cache
+    // row) leaves the ring buffer by one bulk store issued by thread 0.
     const bool ok = mbar_wait_warp(&full[b], (phase_bits >> b) & 1u, abort_flag, a.err);
+    if (ok && tid == 0 && slot_ok) {
+      uint8_t* v_dst = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(a.v_cache) + crow * a.n_kv * D);
+      const uint8_t* v_src = smem + b * L.raw_stride + static_cast<size_t>(qk_vec) * 16;
+      const uint32_t v_bytes = static_cast<uint32_t>(a.n_kv * D * 2);
+      for (uint32_t off = 0; off < v_bytes; off += kBulkChunk)
+        bulk_store(v_dst + off, v_src + off, v_bytes - off < kBulkChunk ? v_bytes - off : kBulkChunk);
+      bulk_commit();
+    }
     float ss_q = 0.f, ss_k = 0.f;
     if (ok && worker) {
       int v = tid;
@@ -534,19 +543,6 @@ qkv_staged_kernel(const __grid_constant__ QkvArgs a) {
       for (; v < qk_vec; v += active)
         stage_vector<FULL>(a, v, lds128(raw32 + v * 16), ld_cached(wptr(v)), u32 + v * 32, own_lo_b, own_hi_b, q_vec,
                            vph, lg_vph, inv_head, ss_q, ss_k);
-      if (slot_ok) {
-        __nv_bfloat16* v_dst =
-            static_cast<__nv_bfloat16*>(a.v_cache) + crow * a.n_kv * D - static_cast<int64_t>(qk_vec) * 8;
-        int w = qk_vec + tid;
-        for (; w + (kStagedUnroll - 1) * active < all_vec; w += kStagedUnroll * active) {
-          uint4 xv[kStagedUnroll];
-#pragma unroll
-          for (int k = 0; k < kStagedUnroll; ++k) xv[k] = lds128(raw32 + (w + k * active) * 16);
-#pragma unroll
-          for (int k = 0; k < kStagedUnroll; ++k) st_16(v_dst + (w + k * active) * 8, xv[k]);
-        }
-        for (; w < all_vec; w += active) st_16(v_dst + w * 8, lds128(raw32 + w * 16));
-      }
     }
     if (FULL) {
       ss_q = warp_sum(ss_q);
@@ -559,6 +555,7 @@ qkv_staged_kernel(const __grid_constant__ QkvArgs a) {
     if (__syncthreads_or(!ok)) {
       // A row never arrived: wait (bounded) for the copies still in flight, then leave.
       if (tid == 0) {
+        bulk_wait_all();
         int give_up = 0;
         for (int j = 0, bj = b; j < nb; ++j, bj = bj + 1 == nb ? 0 : bj + 1) {
           if (t + static_cast<int64_t>(j) * gridDim.x >= a.tokens) break;
@@ -571,6 +568,7 @@ qkv_staged_kernel(const __grid_constant__ QkvArgs a) {
     if (tid == 0) {
       const int64_t tn = t + static_cast<int64_t>(nb) * gridDim.x;
       if (tn < a.tokens) {
+        bulk_wait_read_all();       // the V store has read its part of the buffer
         fence_proxy_async_smem();   // the barrier ordered every thread's reads of the buffer before this
         load_row(smem + b * L.raw_stride, qkv + tn * row_bytes, row_bytes, &full[b]);
       }
@@ -627,6 +625,7 @@ qkv_staged_kernel(const __grid_constant__ QkvArgs a) {
     }
     __syncthreads();
   }
+  if (tid == 0) bulk_wait_all();     // the last V stores have completed
 }
 
 int gcd_int(int x, int y) {
