@@ -93,11 +93,16 @@ __global__ void __launch_bounds__(kBnBlock) fold_norm_weight_kernel(const NormFo
     if (VEC) {
       const int nvec = static_cast<int>(a.inner >> 3);
       for (int base = 0; base < nvec; base += 32 * kBnUnroll) {
-        uint4 v[kBnUnroll];
+        // the gamma vectors (L1-resident, shared by every row) are requested
+        // with the row's vectors, not after them
+        uint4 v[kBnUnroll], gq[kBnUnroll];
 #pragma unroll
         for (int k = 0; k < kBnUnroll; ++k) {
           const int i = base + k * 32 + lane;
-          if (i < nvec) v[k] = ld_stream(src + i * 8);
+          if (i < nvec) {
+            v[k] = ld_stream(src + i * 8);
+            gq[k] = ld_cached(gam + i * 8);
+          }
         }
 #pragma unroll
         for (int k = 0; k < kBnUnroll; ++k) {
@@ -105,7 +110,7 @@ __global__ void __launch_bounds__(kBnBlock) fold_norm_weight_kernel(const NormFo
           if (i < nvec) {
             float f[8], gv[8];
             bf16x8_to_f32(v[k], f);
-            bf16x8_to_f32(ld_cached(gam + i * 8), gv);
+            bf16x8_to_f32(gq[k], gv);
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(f[e], g_of(gv[e]));
             st_16(dst + i * 8, f32x8_to_bf16x8(f));
