@@ -508,10 +508,13 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
               for (int e = 0; e < 8; ++e) sc[e] = p.x_scale * ws[e];
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float acc = __uint_as_float(r[g * 8 + e]);
-              const float a = FP8 ? fmaf(acc, sc[e], bz[e]) : acc + bz[e];
-              v[e] = fast_act(a, p.act);
+            for (int e = 0; e < 8; e += 2) {
+              const float2 acc = make_float2(__uint_as_float(r[g * 8 + e]), __uint_as_float(r[g * 8 + e + 1]));
+              const float2 bb = make_float2(bz[e], bz[e + 1]);
+              const float2 a = FP8 ? __ffma2_rn(acc, make_float2(sc[e], sc[e + 1]), bb) : __fadd2_rn(acc, bb);
+              const float2 o = fast_act2(a, p.act);
+              v[e] = o.x;
+              v[e + 1] = o.y;
             }
             // 16-byte piece j of row `lane` sits at piece j ^ (row % 8) (the TMA 128-byte swizzle)
             const int j = sub * 4 + g;
