@@ -120,8 +120,12 @@ def test_3d_per_head_with_zero_section(gbf):
     check(gbf, c, "3D with an empty section")
 
 
-def test_slots_scatter_into_a_larger_cache(gbf):
-    c = workloads.qkv_case(12, 4, 2, 128, 0, 0, seed=9, theta=1e6)
+@pytest.mark.parametrize("norm,rope", [(0, 0), (1, 1)])
+def test_slots_scatter_into_a_larger_cache(gbf, norm, rope):
+    """Arbitrary cache rows per token (a paged cache's slot mapping), on the
+    per-head kernel and on the staged kernel, whose V leaves by bulk store."""
+    c = workloads.qkv_case(12, 4, 2, 128, norm, rope, seed=9 + norm, theta=1e6 if rope == 0 else 1e4,
+                           grid=(2, 2, 3) if rope else None, sections=(44, 42, 42) if rope else None)
     slots = np.random.default_rng(3).permutation(40)[:12].astype(np.int32)
     q, kc, vc = run_gpu(gbf, c, slots=slots, cache_rows=40)
     rq, rk, rv = run_oracle(c, slots=slots, cache_rows=40)
