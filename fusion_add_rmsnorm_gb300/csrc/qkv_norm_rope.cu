@@ -27,19 +27,21 @@
 // position 4095, where a plain binary32 product would be 2.4e-4 rad off.
 //
 // Two kernels:
-//  * qkv_rot1d_kernel (per-head norm, 1D, head_dim 64/128/256): D/16 lanes
-//    own a head; lane l holds the 16-byte vectors l and l + D/16, which contain
-//    both members of its 8 rotation pairs (j, j + D/2), so the rotation is done
-//    in registers and the head's sum of squares is a shuffle reduction over the
-//    head's lanes.  Each thread visits every 8th head of its token (V heads are
-//    copied), issuing a batch of loads before any arithmetic, and computes the
-//    (cos, sin) of its 8 slots once per token.
+//  * qkv_rot1d_kernel (per-head RMSNorm or LayerNorm, 1D, head_dim 64/128/
+//    256): D/16 lanes own a head; lane l holds the 16-byte vectors l and
+//    l + D/16, which contain both members of its 8 rotation pairs (j, j + D/2),
+//    so the rotation is done in registers and the head's statistics are a
+//    shuffle reduction over the head's lanes.  Each thread visits every G-th
+//    head of its token (G = 8, 16 or 32 head groups; V heads are copied),
+//    issuing a batch of loads before any arithmetic, and the token's (cos, sin)
+//    are computed once per token into a shared table.
 //  * qkv_staged_kernel (everything else: full-width norm and/or 3D sections,
 //    where a rotation pair need not sit in one 16-byte vector): a persistent
 //    CTA streams its tokens' packed rows through a ring of shared-memory
-//    buffers filled by bulk copies.  Per token, phase 1 copies V out and writes
-//    x * w of Q and K to shared memory as float32 while the sums of squares
-//    are reduced; after one barrier each thread takes its own 16-byte vectors
+//    buffers filled by bulk copies.  Per token, thread 0 sends V out with one
+//    bulk shared-to-global copy while phase 1 writes x * w of Q and K to
+//    shared memory as float32 and reduces the sums of squares; after one
+//    barrier each thread takes its own 16-byte vectors
 //    again, reads the 8 rotation partners of their elements, and stores the
 //    rotated, normalised vector with one 16-byte store.
 #include <map>
