@@ -609,16 +609,41 @@ def kernel_traffic(op_name):
     return ent["dram_bytes_per_launch"]
 
 
+def strip_comments(text):
+    """C/C++/CUDA source without its comments and with runs of whitespace
+    collapsed (string and character literals are kept as written)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            i = text.find("*/", i + 2)
+            i = n if i < 0 else i + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(source):
     """First 16 hex digits of the SHA-256 of a kernel source followed by the
-    headers every kernel includes (a change to either invalidates its record)."""
+    headers every kernel includes, comments and layout stripped (a change to
+    the code of either invalidates its record; a comment edit does not)."""
     csrc = os.path.join(ROOT, "fusion_add_rmsnorm_gb300", "csrc")
     h = hashlib.sha256()
     for name in (source, "common.cuh", "tma.cuh", "kernels.h"):
         path = os.path.join(csrc, name)
         if not os.path.exists(path):
             return None
-        h.update(open(path, "rb").read())
+        h.update(strip_comments(open(path, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 
