@@ -205,6 +205,14 @@ def test_layernorm_shapes(gbf, d, biases, tokens, hq, hkv):
     check_ln(gbf, c, f"LN d {d} biases {biases} [{tokens},{hq},{hkv}]")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_layernorm_many_heads(gbf, d):
+    """More heads than one batch per thread holds (64 + 2 x 32 heads): every
+    thread of the token takes several batches in turn."""
+    c = workloads.layernorm_qkv_case(5, 64, 32, d, seed=91 + d, biases=True)
+    check_ln(gbf, c, f"LN many heads d {d}")
+
+
 def test_layernorm_of_constant_heads_is_the_bias(gbf):
     """Every Q and K head constant: the LayerNorm output is exactly the bias,
     and at position 0 the rotation leaves it alone."""
