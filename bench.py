@@ -657,12 +657,13 @@ KERNEL_FILE = {"add_rmsnorm_fp8": "add_rmsnorm_fp8.cu", "pi05_ada_chain": "add_r
 
 # -------------------------------------------------------------- CPU baseline
 
-def cpu_baseline_sample(scale=1):
+def cpu_baseline_sample(scale=1, gemm=True):
     """Time the oracle's unfused chains on a bounded sample of every operator
     of the step, single-threaded, and scale to GB/s of algorithmic bytes.
     Returns a dict; runs in a fresh subprocess (see run_cpu_baseline)."""
     import workloads
     from oracle import chains
+    t_start = time.time()
     res = {}
     t_total = 0.0
     byts_total = 0
@@ -713,21 +714,22 @@ def cpu_baseline_sample(scale=1):
     dt = timed(lambda: chains.qkv_split_norm_rope(c["qkv"], 40, 40, 128, 1, c["q_w"], c["k_w"], c["eps"], 1,
                                                   c["pos"], c["theta"], sections=c["sections"]))
     res["wan_qkv3d"] = (bytes_qkv(tw, 40, 40, 128, 1, 1), dt)
-    mg = 16 * scale
-    c = workloads.linear_gelu_case(mg, 16384, 4096, seed=0)
-    dt = timed(lambda: chains.linear_bias_gelu(c["x"], c["w"], c["bias"]))
-    res["linear_bias_gelu"] = (2 * mg * 16384 * 4096, dt)         # flops
-    mf = 16 * scale
-    c = workloads.fp8_linear_case(mf, 16384, 4096, seed=0)
-    import torch
+    if gemm:                       # GFLOP/s only; not part of the GB/s value
+        mg = 16 * scale
+        c = workloads.linear_gelu_case(mg, 16384, 4096, seed=0)
+        dt = timed(lambda: chains.linear_bias_gelu(c["x"], c["w"], c["bias"]))
+        res["linear_bias_gelu"] = (2 * mg * 16384 * 4096, dt)         # flops
+        mf = 16 * scale
+        c = workloads.fp8_linear_case(mf, 16384, 4096, seed=0)
+        import torch
 
-    def e4m3(v):   # input codes (outside the timed call): clamp, then torch's nearest-even conversion
-        return torch.from_numpy(np.ascontiguousarray(v, np.float32)).clamp(-448, 448).to(
-            torch.float8_e4m3fn).view(torch.uint8).numpy()
-    xq = e4m3(c["x"] / np.float32(c["x_scale"]))
-    wq = e4m3(c["w"] / c["w_scale"][:, None])
-    dt = timed(lambda: chains.linear_fp8_act(xq, np.float32(c["x_scale"]), wq, c["w_scale"], c["bias"], act=1))
-    res["linear_fp8_gelu"] = (2 * mf * 16384 * 4096, dt)       # flops
+        def e4m3(v):   # input codes (outside the timed call): clamp, then torch's nearest-even conversion
+            return torch.from_numpy(np.ascontiguousarray(v, np.float32)).clamp(-448, 448).to(
+                torch.float8_e4m3fn).view(torch.uint8).numpy()
+        xq = e4m3(c["x"] / np.float32(c["x_scale"]))
+        wq = e4m3(c["w"] / c["w_scale"][:, None])
+        dt = timed(lambda: chains.linear_fp8_act(xq, np.float32(c["x_scale"]), wq, c["w_scale"], c["bias"], act=1))
+        res["linear_fp8_gelu"] = (2 * mf * 16384 * 4096, dt)       # flops
     cf = 1024 * scale
     c = workloads.norm_fold_case(cf, 4096)
     dt = timed(lambda: chains.fold_norm_weight_bf16(c["w"], c["gamma"]))
@@ -740,28 +742,62 @@ def cpu_baseline_sample(scale=1):
         if k not in ("linear_bias_gelu", "linear_fp8_gelu"):
             t_total += dt
             byts_total += b
-    return {"gbs": byts_total / t_total / 1e9, "seconds": t_total,
+    return {"gbs": byts_total / t_total / 1e9, "seconds": t_total, "bytes": byts_total, "t_start": t_start,
             "per_op": {k: ({"gflops": b / dt / 1e9} if k in ("linear_bias_gelu", "linear_fp8_gelu") else {"gbs": b / dt / 1e9})
                        for k, (b, dt) in res.items()}}
 
 
-def run_cpu_baseline(scale=32):
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_cpu_baseline(scale=32, all_cores=True):
+    """The oracle's bounded sample in one single-threaded child process; then,
+    with all_cores, one such child per host core running a quarter of that
+    sample's memory-bound operators at the same time (every child starts its
+    timed work at one shared wall-clock instant, after its imports), reported
+    as the aggregate over the cores."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_cpu-baseline-child", str(scale)], env=env,
-                       capture_output=True, text=True, timeout=600)
+    cmd = [sys.executable, os.path.abspath(__file__), "--_cpu-baseline-child"]
+    r = subprocess.run(cmd + [str(scale)], env=env, capture_output=True, text=True, timeout=600)
     if r.returncode != 0:
         return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": r.stderr[-300:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": round(d["gbs"], 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": (f"float64 numpy oracle, one thread: [16,256] add+RMSNorm+FP8; {min(10 * scale, 180)} of the 180 "
-                       f"chained [10,1024] AdaRMSNorm calls; {64 * scale} rows of each [65536,4096] sweep; "
-                       f"{256 * scale} Qwen3 tokens; {128 * scale} Chameleon tokens; {16 * scale} SwiGLU rows; "
-                       f"{64 * scale} Wan tokens; "
-                       f"BN fold and norm-weight fold of {1024 * scale} channels each; "
-                       "GB/s = algorithmic bytes / oracle time over the memory-bound operators (a "
-                       f"{16 * scale}-row sample of each GEMM is in per_op as GFLOP/s)"),
-            "seconds": round(d["seconds"], 3), "per_op": d["per_op"]}
+    out = {"value": round(d["gbs"], 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": (f"float64 numpy oracle, one thread per process: [16,256] add+RMSNorm+FP8; {min(10 * scale, 180)} of "
+                      f"the 180 chained [10,1024] AdaRMSNorm calls; {64 * scale} rows of each [65536,4096] sweep; "
+                      f"{256 * scale} Qwen3 tokens; {128 * scale} Chameleon tokens; {16 * scale} SwiGLU rows; "
+                      f"{64 * scale} Wan tokens; "
+                      f"BN fold and norm-weight fold of {1024 * scale} channels each; "
+                      "GB/s = algorithmic bytes / oracle time over the memory-bound operators (a "
+                      f"{16 * scale}-row sample of each GEMM is in per_op as GFLOP/s)"),
+           "seconds": round(d["seconds"], 3), "per_op": d["per_op"]}
+    cores = host_cores()
+    if not all_cores or cores < 2:
+        return out
+    part = max(1, scale // 4)
+    start = time.time() + 8.0
+    procs = [subprocess.Popen(cmd + [str(part), "--_cpu-baseline-start", f"{start:.3f}", "--_cpu-baseline-nogemm"],
+                              env=env,
+                              stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True) for _ in range(cores)]
+    results = []
+    for pr in procs:
+        so, se = pr.communicate(timeout=900)
+        if pr.returncode == 0:
+            results.append(json.loads(so.strip().splitlines()[-1]))
+    if len(results) == cores:
+        agg = sum(x["bytes"] for x in results) / max(x["seconds"] for x in results) / 1e9
+        out["start_spread_s"] = round(max(x["t_start"] for x in results) - min(x["t_start"] for x in results), 3)
+        out["one_core"] = {"value": out["value"], "seconds": out["seconds"]}
+        out["value"] = round(agg, 4)
+        out["cores"] = cores
+        out["sample"] += (f"; all cores: {cores} such processes at once, each on a quarter of the memory-bound sample, "
+                          "value = their summed bytes / the slowest one's oracle time")
+    return out
 
 
 # ------------------------------------------------------------------ main arm
@@ -1000,7 +1036,7 @@ def main_reference(args):
     vals = []
     res = None
     for i in range(args.warmup + args.steps):
-        res = run_cpu_baseline(scale=2)
+        res = run_cpu_baseline(scale=2, all_cores=False)
         if i >= args.warmup:
             times.append(res["seconds"])
             vals.append(res["value"])
@@ -1080,12 +1116,18 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="add+RMSNorm+FP8 over rows {4096, 16384, 65536} x hidden {1024, 4096, 8192} x 3 modes")
     ap.add_argument("--_cpu-baseline-child", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--_cpu-baseline-start", type=float, default=0.0, help=argparse.SUPPRESS)
+    ap.add_argument("--_cpu-baseline-nogemm", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.sweep:
         main_sweep(args)
         return
     if args._cpu_baseline_child:
-        print(json.dumps(cpu_baseline_sample(args._cpu_baseline_child)))
+        if args._cpu_baseline_start:
+            import workloads  # noqa: F401  (imports done before the shared start)
+            from oracle import chains  # noqa: F401
+            time.sleep(max(0.0, args._cpu_baseline_start - time.time()))
+        print(json.dumps(cpu_baseline_sample(args._cpu_baseline_child, gemm=not args._cpu_baseline_nogemm)))
         return
     if args.impl == "reference":
         main_reference(args)
