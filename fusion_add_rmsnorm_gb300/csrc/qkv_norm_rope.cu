@@ -264,16 +264,22 @@ GBF_DEVICE void rot1d_cs_read(const float4* cs_tok, int lane, float2 (&c2)[4], f
   }
 }
 
+// Threads per CTA of the per-head kernel: 128 where a token's G * LPH threads
+// fit, else 256.  The smaller CTA ends sooner (its share of the bandwidth
+// moves fewer tokens), so the tail of a launch, where the last CTAs run
+// alone, is shorter; the registers per thread are the same either way.
+constexpr int rot1d_block(int g, int lph) { return g * lph <= 128 ? 128 : kRotBlock; }
+
 // One CTA per TOK tokens; a thread with more than one batch of heads takes
 // them in turn.  The first batch is requested before the (cos, sin) table.
-template <int LPH, bool LN, int G>
-__global__ void __launch_bounds__(kRotBlock, LN ? 3 : 4)
+template <int LPH, bool LN, int G, int BLOCK>
+__global__ void __launch_bounds__(BLOCK, (LN ? 3 : 4) * kRotBlock / BLOCK)
 qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   constexpr int D = LPH * 16;
   constexpr int SLOTS = D / 2;
   constexpr int TPT = G * LPH;              // threads per token
-  constexpr int TOK = kRotBlock / TPT;      // tokens per CTA
-  static_assert(TOK * SLOTS <= kRotBlock, "at most one (cos, sin) per thread");
+  constexpr int TOK = BLOCK / TPT;          // tokens per CTA
+  static_assert(TOK >= 1 && TOK * SLOTS <= BLOCK, "a token fits the CTA, at most one (cos, sin) per thread");
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x % LPH;
@@ -706,12 +712,13 @@ cudaError_t launch_staged(const QkvArgs& a, cudaStream_t stream) {
 
 template <int LPH, int G>
 cudaError_t launch_rot1d_g(const QkvArgs& a, cudaStream_t stream) {
-  static_assert(G * LPH <= kRotBlock, "a token's threads fit one CTA");
-  const int tok_per_cta = kRotBlock / (G * LPH);
+  constexpr int BLOCK = rot1d_block(G, LPH);
+  static_assert(G * LPH <= BLOCK, "a token's threads fit one CTA");
+  const int tok_per_cta = BLOCK / (G * LPH);
   const unsigned grid = static_cast<unsigned>((a.tokens + tok_per_cta - 1) / tok_per_cta);
   if (a.norm == kQkNormLayerNorm)
-    return launch_pdl(qkv_rot1d_kernel<LPH, true, G>, dim3(grid), dim3(kRotBlock), 0, stream, a);
-  return launch_pdl(qkv_rot1d_kernel<LPH, false, G>, dim3(grid), dim3(kRotBlock), 0, stream, a);
+    return launch_pdl(qkv_rot1d_kernel<LPH, true, G, BLOCK>, dim3(grid), dim3(BLOCK), 0, stream, a);
+  return launch_pdl(qkv_rot1d_kernel<LPH, false, G, BLOCK>, dim3(grid), dim3(BLOCK), 0, stream, a);
 }
 
 // G = the smallest of 8, 16, 32 head groups that leaves a thread at most
