@@ -165,8 +165,11 @@ GBF_API int gbf_qkv_split_layernorm_rope(const void* qkv, int64_t tokens, int n_
  * sqrt 2)), the exact GELU of RFC §3.6) or GBF_ACT_SILU (a / (1 + exp(-a))).
  * Requires K % 64 == 0, N % 16 == 0, M >= 1 and 16-byte aligned X, W, Y
  * (GBF_EUNSUPPORTED / GBF_EALIGN otherwise); Y may not overlap X, W or bias.
- * The kernel's pipeline waits are bounded: a wait that gives up sets the
- * device error word (gbf_device_status() returns GBF_ETIMEOUT).
+ * One launch: when M spans more than one 128-row tile, clusters of two CTAs
+ * run as tcgen05 CTA pairs on adjacent 128-row tiles.  The kernel's pipeline
+ * waits are bounded: a wait that gives up sets the device error word
+ * (gbf_device_status() returns GBF_ETIMEOUT); a CTA pair handed two different
+ * tensor-memory bases does no work and sets it too (GBF_EDEVICE).
  */
 GBF_API int gbf_linear_bias_gelu(const void* X, const void* W, const void* bias, void* Y, int64_t M,
                                  int64_t N, int64_t K, int act, void* stream);
