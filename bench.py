@@ -914,9 +914,10 @@ def main_gpu(args):
     out_ops = {}
     for name, d in per_op.items():
         op = d["op"]
-        ms = sum(d["ms"]) / len(d["ms"])
+        ms = sum(d["ms"]) / len(d["ms"])       # the mean: whole-job time over the timed steps
         step_ms += ms
-        entry = {"ms": round(ms, 5), "launches": op.launches, "tokens_per_s": round(op.units() / (ms / 1e3), 1)}
+        entry = {"ms": round(ms, 5), "ms_median": round(statistics.median(d["ms"]), 5), "launches": op.launches,
+                 "tokens_per_s": round(op.units() / (ms / 1e3), 1)}
         if op.bound == "tensor":
             tf = op.flops() / (ms / 1e3) / 1e12
             peak = peaks["bf16_tflops"] * getattr(op, "peak_ratio", 1.0)
@@ -1106,7 +1107,7 @@ def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-gemm", action="store_true", help="leave the GEMM row out of the step")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
