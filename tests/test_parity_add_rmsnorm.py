@@ -117,3 +117,31 @@ def test_large_launch_plans_sampled_rows(gbf, mode, rows, hidden):
     c = workloads.add_rmsnorm_case(rows, hidden, mode, seed=rows + hidden + mode, gated=mode == 2)
     pick = np.unique(np.concatenate([[0, rows - 1], np.random.default_rng(mode).choice(rows, 62, replace=False)]))
     check(gbf, c, rows=pick, what=f"[{rows},{hidden}] mode {mode}")
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_fused_codes_at_least_as_close_as_the_unfused_chain(gbf, mode):
+    """FlashRT's acceptance check: the fused path's cosine to the exact result
+    is no worse than the unfused chain's.  The unfused chain stores y in bf16
+    before the quantiser (one more rounding); the fused kernel quantises the
+    float32 y.  Both sets of codes, dequantised, against the exact float64 y."""
+    from oracle import formats, ops
+    c = workloads.add_rmsnorm_case(64, 4096, mode, seed=500 + mode, gated=(mode == 2))
+    res_out, q = run_gpu(gbf, c)
+    _, q_unfused = chains.add_rmsnorm_fp8(c["x"], c["res"], c["eps"], c["s_q"], mode, weight=c["weight"],
+                                          gate=c["gate"], ada_scale=c["scale"], ada_shift=c["shift"],
+                                          round_y_bf16=True)
+    r_hat = formats.bf16_decode(res_out)
+    n = ops.rmsnorm(r_hat, c["eps"])
+    if mode == 0:
+        y = n * formats.bf16_decode(c["weight"])[None, :]
+    elif mode == 1:
+        y = n
+    else:
+        y = ops.ada_modulate(n, formats.bf16_decode(c["scale"])[None, :], formats.bf16_decode(c["shift"])[None, :])
+    y = np.clip(y / c["s_q"], -448.0, 448.0).ravel()
+
+    def cos(codes):
+        d = formats.e4m3_decode(codes).astype(np.float64).ravel()
+        return float(d @ y / np.linalg.norm(d) / np.linalg.norm(y))
+    assert cos(q) >= cos(q_unfused) - 1e-9, (cos(q), cos(q_unfused))
