@@ -69,8 +69,25 @@ def _check(status):
     return status
 
 
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+_BF16, _U8, _I32, _F32 = torch.bfloat16, torch.uint8, torch.int32, torch.float32
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    """Device pointer of a tensor argument after the checks the C ABI cannot
+    make from a raw pointer: a torch tensor on a CUDA device, dense, of the
+    element type the call reads (dtype None: any).  None passes through (an
+    optional argument)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):
@@ -90,11 +107,15 @@ def raw():
 
 def add_rmsnorm_fp8(x, res_in, res_out, q_out, mode, weight=None, gate=None, ada_scale=None, ada_shift=None,
                     eps=1e-6, fp8_scale=0.05, stream=None):
-    """gbf_add_rmsnorm_fp8 on [rows, hidden] bf16 tensors; q_out is uint8."""
-    rows, hidden = x.shape[0], x.shape[-1]
-    return _check(_lib.gbf_add_rmsnorm_fp8(_ptr(x), _ptr(res_in), _ptr(res_out), _ptr(gate), mode, _ptr(weight),
-                                           _ptr(ada_scale), _ptr(ada_shift), _ptr(q_out), rows, hidden, eps,
-                                           fp8_scale, _stream(stream)))
+    """gbf_add_rmsnorm_fp8 on [..., hidden] bf16 tensors (rows = every leading
+    index); q_out is uint8 E4M3 codes of the same shape."""
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden if hidden else 0
+    return _check(_lib.gbf_add_rmsnorm_fp8(_ptr(x, _BF16, "x"), _ptr(res_in, _BF16, "res_in"),
+                                           _ptr(res_out, _BF16, "res_out"), _ptr(gate, _BF16, "gate"), mode,
+                                           _ptr(weight, _BF16, "weight"), _ptr(ada_scale, _BF16, "ada_scale"),
+                                           _ptr(ada_shift, _BF16, "ada_shift"), _ptr(q_out, _U8, "q_out"), rows,
+                                           hidden, eps, fp8_scale, _stream(stream)))
 
 
 def qkv_split_norm_rope(qkv, n_q_heads, n_kv_heads, head_dim, norm, q_w, k_w, eps, rope, pos, theta, q_out,
@@ -103,10 +124,12 @@ def qkv_split_norm_rope(qkv, n_q_heads, n_kv_heads, head_dim, norm, q_w, k_w, ep
     tokens = qkv.shape[0]
     sec = None if sections is None else (ctypes.c_int32 * 3)(*sections)
     rows = k_cache.shape[0] if cache_rows is None else cache_rows
-    return _check(_lib.gbf_qkv_split_norm_rope(_ptr(qkv), tokens, n_q_heads, n_kv_heads, head_dim, norm, _ptr(q_w),
-                                               _ptr(k_w), eps, rope, _ptr(pos),
+    return _check(_lib.gbf_qkv_split_norm_rope(_ptr(qkv, _BF16, "qkv"), tokens, n_q_heads, n_kv_heads, head_dim,
+                                               norm, _ptr(q_w, _BF16, "q_w"), _ptr(k_w, _BF16, "k_w"), eps, rope,
+                                               _ptr(pos, _I32, "pos"),
                                                ctypes.cast(sec, ctypes.c_void_p) if sec is not None else None,
-                                               theta, _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(slots),
+                                               theta, _ptr(q_out, _BF16, "q_out"), _ptr(k_cache, _BF16, "k_cache"),
+                                               _ptr(v_cache, _BF16, "v_cache"), _ptr(slots, _I32, "slots"),
                                                rows, _stream(stream)))
 
 
@@ -115,53 +138,63 @@ def qkv_split_layernorm_rope(qkv, n_q_heads, n_kv_heads, head_dim, q_w, q_b, k_w
     """gbf_qkv_split_layernorm_rope: per-head LayerNorm (biases may be None) + 1D RoPE."""
     tokens = qkv.shape[0]
     rows = k_cache.shape[0] if cache_rows is None else cache_rows
-    return _check(_lib.gbf_qkv_split_layernorm_rope(_ptr(qkv), tokens, n_q_heads, n_kv_heads, head_dim, _ptr(q_w),
-                                                    _ptr(q_b), _ptr(k_w), _ptr(k_b), eps, _ptr(pos), theta,
-                                                    _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(slots), rows,
-                                                    _stream(stream)))
+    return _check(_lib.gbf_qkv_split_layernorm_rope(_ptr(qkv, _BF16, "qkv"), tokens, n_q_heads, n_kv_heads,
+                                                    head_dim, _ptr(q_w, _BF16, "q_w"), _ptr(q_b, _BF16, "q_b"),
+                                                    _ptr(k_w, _BF16, "k_w"), _ptr(k_b, _BF16, "k_b"), eps,
+                                                    _ptr(pos, _I32, "pos"), theta, _ptr(q_out, _BF16, "q_out"),
+                                                    _ptr(k_cache, _BF16, "k_cache"), _ptr(v_cache, _BF16, "v_cache"),
+                                                    _ptr(slots, _I32, "slots"), rows, _stream(stream)))
 
 
 def linear_bias_gelu(x, w, bias, y, act=ACT_GELU_TANH, stream=None):
-    """gbf_linear_bias_gelu: y[M, N] = act(x[M, K] @ w[N, K]^T + bias[N])."""
-    m, k = x.shape
+    """gbf_linear_bias_gelu: y[..., N] = act(x[..., K] @ w[N, K]^T + bias[N])."""
+    k = x.shape[-1]
+    m = x.numel() // k if k else 0
     n = w.shape[0]
-    return _check(_lib.gbf_linear_bias_gelu(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), m, n, k, act, _stream(stream)))
+    return _check(_lib.gbf_linear_bias_gelu(_ptr(x, _BF16, "x"), _ptr(w, _BF16, "w"), _ptr(bias, _BF16, "bias"),
+                                            _ptr(y, _BF16, "y"), m, n, k, act, _stream(stream)))
 
 
 def linear_fp8_act(xq, x_scale, wq, w_scale, bias, y, act=ACT_GELU_TANH, stream=None):
     """gbf_linear_fp8_act: y[M, N] = act((xq * x_scale) @ (wq * w_scale[:, None])^T + bias); xq, wq uint8 codes."""
-    m, k = xq.shape
+    k = xq.shape[-1]
+    m = xq.numel() // k if k else 0
     n = wq.shape[0]
-    return _check(_lib.gbf_linear_fp8_act(_ptr(xq), x_scale, _ptr(wq), _ptr(w_scale), _ptr(bias), _ptr(y), m, n, k,
-                                          act, _stream(stream)))
+    return _check(_lib.gbf_linear_fp8_act(_ptr(xq, _U8, "xq"), x_scale, _ptr(wq, _U8, "wq"),
+                                          _ptr(w_scale, _F32, "w_scale"), _ptr(bias, _BF16, "bias"),
+                                          _ptr(y, _BF16, "y"), m, n, k, act, _stream(stream)))
 
 
 def fold_norm_weight(w, gamma, w_out, gemma_style=True, stream=None):
     """gbf_fold_norm_weight: w_out = w * (1 + gamma) (or w * gamma), per column."""
     out_ch = w.shape[0]
     inner = w.numel() // max(out_ch, 1)
-    return _check(_lib.gbf_fold_norm_weight(_ptr(w), _ptr(gamma), 1 if gemma_style else 0, out_ch, inner,
-                                            _ptr(w_out), _stream(stream)))
+    return _check(_lib.gbf_fold_norm_weight(_ptr(w, _BF16, "w"), _ptr(gamma, _BF16, "gamma"),
+                                            1 if gemma_style else 0, out_ch, inner, _ptr(w_out, _BF16, "w_out"),
+                                            _stream(stream)))
 
 
 def gated_act(x, y, act=ACT_SILU, stream=None):
     """gbf_gated_act: y[rows, d] = act(x[:, :d]) * x[:, d:] for x [rows, 2d]."""
-    rows, d = y.shape[0], y.shape[-1]
-    return _check(_lib.gbf_gated_act(_ptr(x), _ptr(y), rows, d, act, _stream(stream)))
+    d = y.shape[-1]
+    rows = y.numel() // d if d else 0
+    return _check(_lib.gbf_gated_act(_ptr(x, _BF16, "x"), _ptr(y, _BF16, "y"), rows, d, act, _stream(stream)))
 
 
 def bn_fold(w, b, gamma, beta, mean, var, eps, w_out, b_out, stream=None):
     """gbf_bn_fold on a weight [out_ch, ...] (flattened per output channel)."""
     out_ch = w.shape[0]
     inner = w.numel() // max(out_ch, 1)
-    return _check(_lib.gbf_bn_fold(_ptr(w), _ptr(b), _ptr(gamma), _ptr(beta), _ptr(mean), _ptr(var), eps, out_ch,
-                                   inner, _ptr(w_out), _ptr(b_out), _stream(stream)))
+    return _check(_lib.gbf_bn_fold(_ptr(w, _BF16, "w"), _ptr(b, _BF16, "b"), _ptr(gamma, _F32, "gamma"),
+                                   _ptr(beta, _F32, "beta"), _ptr(mean, _F32, "mean"), _ptr(var, _F32, "var"), eps,
+                                   out_ch, inner, _ptr(w_out, _BF16, "w_out"), _ptr(b_out, _BF16, "b_out"),
+                                   _stream(stream)))
 
 
 def copy(src, dst, nbytes=None, stream=None):
     """gbf_copy of nbytes (default: all of src) bytes."""
     n = src.numel() * src.element_size() if nbytes is None else nbytes
-    return _check(_lib.gbf_copy(_ptr(src), _ptr(dst), n, _stream(stream)))
+    return _check(_lib.gbf_copy(_ptr(src, None, "src"), _ptr(dst, None, "dst"), n, _stream(stream)))
 
 
 def selftest_bounded_wait(stream=None):

@@ -203,9 +203,12 @@ def test_linear_and_fold_and_copy_validation(gbf):
 
 
 def test_python_binding_raises_with_message(gbf):
-    import torch
-    x = torch.zeros(4, 60, dtype=torch.bfloat16)        # host tensor: validation fails before any launch
+    """A non-OK status from the library becomes GbfError with the status and the
+    library's message: hidden = 60 is not a multiple of 8 (GBF_EALIGN), found on
+    the host before any launch (the pointers are distinct, aligned, never read)."""
+    import ctypes
+    p = [ctypes.c_void_p(a) for a in (1 << 20, 2 << 20, 3 << 20, 4 << 20)]
     with pytest.raises(gbf.GbfError) as e:
-        gbf.add_rmsnorm_fp8(x, x, x.clone(), torch.zeros(4, 60, dtype=torch.uint8), gbf.NORM_NOWEIGHT,
-                            stream=type("S", (), {"cuda_stream": 0})())
-    assert e.value.status == gbf.EALIGN
+        gbf._check(gbf.raw().gbf_add_rmsnorm_fp8(p[0], p[1], p[2], None, gbf.NORM_NOWEIGHT, None, None, None, p[3],
+                                                 4, 60, 1e-6, 0.05, None))
+    assert e.value.status == gbf.EALIGN and len(str(e.value)) > len("status -2: ")
