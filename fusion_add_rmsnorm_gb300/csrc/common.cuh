@@ -1,8 +1,10 @@
 // Shared device helpers for the fused kernels (sm_103a).
 //
 // Storage formats: bfloat16 activations and weights, OCP FP8 E4M3 codes,
-// float32 arithmetic in registers.  Every helper here is a thin wrapper over a
-// CUDA intrinsic; no math-library routine is re-implemented.
+// float32 arithmetic in registers.  The helpers wrap CUDA intrinsics and PTX
+// instructions; the one formula written out, the fast erf, follows a
+// published approximation (cited where it is defined), and no math-library
+// routine is re-implemented.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -139,15 +141,8 @@ GBF_DEVICE float segment_sum(float v, int width) {
 
 // ------------------------------------------------------------ activations
 
-// GELU, tanh form 0.5 a (1 + tanh(0.7978845608 (a + 0.044715 a^3))).
-GBF_DEVICE float act_gelu_tanh(float a) {
-  const float inner = 0.7978845608f * fmaf(0.044715f * a, a * a, a);
-  return 0.5f * a * (1.0f + tanhf(inner));
-}
-// GELU, exact form 0.5 a (1 + erf(a / sqrt 2)).
+// GELU, exact form 0.5 a (1 + erf(a / sqrt 2)), with the library erff.
 GBF_DEVICE float act_gelu_erf(float a) { return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f)); }
-// SiLU a / (1 + exp(-a)); for very negative a the quotient is a signed zero.
-GBF_DEVICE float act_silu(float a) { return a / (1.0f + expf(-a)); }
 
 // Fast forms for epilogues, well inside one bf16 rounding:
 //  * tanh GELU with the hardware tanh approximation (tanh.approx.f32, relative
@@ -199,16 +194,6 @@ GBF_DEVICE float2 fast_act2(float2 a, int act) {
     return __ffma2_rn(h, t, h);
   }
   return make_float2(fast_act(a.x, act), fast_act(a.y, act));
-}
-
-// kActNone / kActGeluTanh / kActGeluErf / kActSilu (the enum of kernels.h).
-GBF_DEVICE float apply_act(float a, int act) {
-  switch (act) {
-    case 1: return act_gelu_tanh(a);
-    case 2: return act_gelu_erf(a);
-    case 3: return act_silu(a);
-    default: return a;
-  }
 }
 
 // --------------------------------------------- programmatic dependent launch

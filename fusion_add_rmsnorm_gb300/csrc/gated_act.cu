@@ -27,11 +27,10 @@ namespace {
 constexpr int kGaBlock = 256;
 constexpr int kGaUnroll = 4;
 
+// SiLU and tanh GELU by the fast forms; erf GELU with the library erff.
 template <int ACT>
 GBF_DEVICE float gate_act(float a) {
-  if (ACT == kActSilu) return __fdividef(a, 1.0f + __expf(-a));
-  if (ACT == kActGeluTanh) return 0.5f * a * (1.0f + tanh_approx(0.7978845608f * fmaf(0.044715f * a, a * a, a)));
-  return act_gelu_erf(a);
+  return ACT == kActGeluErf ? act_gelu_erf(a) : fast_act(a, ACT);
 }
 
 template <int ACT>
