@@ -487,22 +487,30 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
         __syncwarp();
 #pragma unroll 1
         for (int sub = 0; sub < kOutCols / 32; ++sub) {
-          uint32_t r[32];
-          tmem_ld_32cols(taddr + cbase + sub * 32, r);      // this lane's row, 32 columns
+          // the 32 columns' bias and weight descales are requested before the
+          // TMEM load, so their latency overlaps it (the same for every lane)
+          uint4 braw[4];
+          float4 sraw[4][2];
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             const int col = col0 + sub * 32 + g * 8;
             const bool in = col < p.n;                      // N % 16 == 0: whole 8-column groups
+            braw[g] = (p.bias && in) ? ld_cached(p.bias + col) : make_uint4(0, 0, 0, 0);
+            if (FP8) {
+              sraw[g][0] = in ? *reinterpret_cast<const float4*>(p.w_scale + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+              sraw[g][1] = in ? *reinterpret_cast<const float4*>(p.w_scale + col + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+          uint32_t r[32];
+          tmem_ld_32cols(taddr + cbase + sub * 32, r);      // this lane's row, 32 columns
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
             float v[8];
-            float bz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (p.bias && in) bf16x8_to_f32(ld_cached(p.bias + col), bz);
+            float bz[8];
+            bf16x8_to_f32(braw[g], bz);
             float sc[8];
             if (FP8) {                                      // descales: activation x weight row
-              float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-              if (in) {
-                s0 = *reinterpret_cast<const float4*>(p.w_scale + col);
-                s1 = *reinterpret_cast<const float4*>(p.w_scale + col + 4);
-              }
+              const float4 s0 = sraw[g][0], s1 = sraw[g][1];
               const float ws[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
               for (int e = 0; e < 8; ++e) sc[e] = p.x_scale * ws[e];
