@@ -50,37 +50,73 @@ METRIC = "fused-kernel HBM GB/s (% of GB300 peak) and tokens/s per fused op"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 512 << 20
 L2_BYTES = 129 * 10**6           # GB300 L2 capacity
+BF16_DENSE_NOMINAL_TFLOPS = 2250.0
 
 # ----------------------------------------------------------------- bytes model
-# Algorithmic bytes per call: every input read once, every output written once.
+# The graph-autofusion article's benefit model (阶段二收益估算): before fusion
+# every operator of the chain reads its inputs from HBM and writes its output
+# back; after fusion the one kernel reads the chain's inputs once and writes
+# its outputs once.  Byte counts per call; N = rows * hidden elements, bf16 = 2
+# bytes, an E4M3 code = 1 byte.
 
 
 def bytes_add_rmsnorm(rows, hidden, mode, gated):
+    """Fused: read x, res (4N), write res_out (2N) and the codes (N), read the
+    [hidden] vectors the mode uses once: 7N + 2H (weight), + 4H (ada scale and
+    shift), + 2H (gate)."""
     n = rows * hidden
     vec = (2 if mode == 0 else 0) + (4 if mode == 2 else 0) + (2 if gated else 0)
     return 7 * n + vec * hidden
 
 
-def bytes_qkv(tokens, hq, hkv, d, norm, rope):
-    io = 2 * tokens * (hq + 2 * hkv) * d * 2
-    w = (2 * d if norm == 0 else (hq + hkv) * d) * 2
-    pos = tokens * (3 if rope else 1) * 4
-    return io + w + pos
-
-
-def bytes_qkv_layernorm(tokens, hq, hkv, d, biases=True):
-    """Per-head LayerNorm variant: the RMSNorm bytes plus the two bias vectors."""
-    return bytes_qkv(tokens, hq, hkv, d, 0, 0) + (2 * d * 2 if biases else 0)
-
-
-def bytes_unfused_add_rmsnorm(rows, hidden, mode):
-    """The unfused chain of separate operators (add, norm, modulate, quant)."""
+def bytes_unfused_add_rmsnorm(rows, hidden, mode, gated):
+    """The chain of separate operators, each reading and writing HBM:
+    gate multiply (x, gate -> g: 4N + 2H), residual add (6N), RMSNorm (r -> n:
+    4N, + 2H for the weight), AdaRMSNorm's * (1 + scale) (4N + 2H) and + shift
+    (4N + 2H), quantise (y -> codes: 3N).  Weighted, ungated: 13N + 2H; the
+    Pi0.5 gated AdaRMSNorm call: 25N + 6H."""
     n = rows * hidden
+    total = (4 * n + 2 * hidden if gated else 0) + 6 * n + 4 * n + 3 * n
     if mode == 0:
-        return 13 * n + 2 * hidden                        # add 6N, norm 4N + 2H, quant 3N
-    if mode == 1:
-        return 13 * n
-    return 6 * n + 6 * n + 4 * n + 6 * n + 6 * n + 3 * n  # mul, add, norm, *(1+s), +shift, quant
+        total += 2 * hidden
+    elif mode == 2:
+        total += 2 * (4 * n + 2 * hidden)
+    return total
+
+
+def bytes_qkv(tokens, hq, hkv, d):
+    """Fused QKV post-processing: read the packed row once, write Q, K and V
+    once: 2 * T * (Hq + 2 Hkv) * D bf16 values.  The norm weights and the
+    positions (under 0.02 % at the configs) are left out, as in the survey's
+    table."""
+    return 2 * tokens * (hq + 2 * hkv) * d * 2
+
+
+def bytes_unfused_qkv(tokens, hq, hkv, d, norm):
+    """Per-head norm (and the LayerNorm variant): the split is a view; Q norm
+    and Q RoPE read and write Q (4q), K norm, K RoPE and the K-cache copy read
+    and write K (6kv), the V-cache copy reads and writes V (2kv).  Full-width
+    norm (Wan): the split reads and writes all three (2 (q + 2kv)), the two
+    norms and the two RoPEs each read and write Q and K (4 (q + kv))."""
+    q, kv = tokens * hq * d * 2, tokens * hkv * d * 2
+    if norm in (0, 2):
+        return 4 * q + 6 * kv + 2 * kv
+    return 2 * (q + 2 * kv) + 2 * (q + kv) + 2 * (q + kv)
+
+
+def bytes_linear(m, n, k, bias=True):
+    """Fused Linear + bias + GELU: read X and W, read the bias, write Y once (bf16)."""
+    return 2 * (m * k + n * k + (n if bias else 0) + m * n)
+
+
+def bytes_unfused_linear(m, n, k):
+    """GEMM (X, W -> Y), bias add (Y, b -> Y: 4MN + 2N), GELU (Y -> Y: 4MN)."""
+    return 2 * (m * k + n * k + m * n) + (4 * m * n + 2 * n) + 4 * m * n
+
+
+def bytes_bn_fold(out_ch, inner):
+    """W read and written (bf16), b read and written, gamma, beta, mean, var read (float32)."""
+    return 2 * out_ch * inner * 2 + 2 * out_ch * 2 + 4 * out_ch * 4
 
 
 def load_peaks():
@@ -156,7 +192,7 @@ class AddRmsNormOp(Op):
         return self.launches * bytes_add_rmsnorm(self.rows, self.hidden, self.mode, self.gated)
 
     def unfused_bytes(self):
-        return self.launches * bytes_unfused_add_rmsnorm(self.rows, self.hidden, self.mode)
+        return self.launches * bytes_unfused_add_rmsnorm(self.rows, self.hidden, self.mode, self.gated)
 
     def units(self):
         return self.launches * self.rows
@@ -216,7 +252,7 @@ class AdaChainOp(Op):
         return self.launches * bytes_add_rmsnorm(10, 1024, 2, True)
 
     def unfused_bytes(self):
-        return self.launches * bytes_unfused_add_rmsnorm(10, 1024, 2)
+        return self.launches * bytes_unfused_add_rmsnorm(10, 1024, 2, True)
 
     def units(self):
         return self.launches * 10
@@ -267,17 +303,11 @@ class QkvOp(Op):
 
     def algorithmic_bytes(self):
         c = self.c
-        if self.ln:
-            return self.launches * bytes_qkv_layernorm(c["tokens"], c["n_q"], c["n_kv"], c["d"], self.qb is not None)
-        return self.launches * bytes_qkv(c["tokens"], c["n_q"], c["n_kv"], c["d"], c["norm"], c["rope"])
+        return self.launches * bytes_qkv(c["tokens"], c["n_q"], c["n_kv"], c["d"])
 
     def unfused_bytes(self):
         c = self.c
-        t, hq, hkv, d = c["tokens"], c["n_q"], c["n_kv"], c["d"]
-        q, kv = t * hq * d * 2, t * hkv * d * 2
-        if c["norm"] in (0, 2):   # views for the split; q norm+rope 4 passes, k norm+rope+cache 6, v cache 2
-            return self.launches * (4 * q + 6 * kv + 2 * kv)
-        return self.launches * (6 * (q + 2 * kv) + 4 * (q + kv) + 4 * (q + kv))   # split, two norms, two ropes
+        return self.launches * bytes_unfused_qkv(c["tokens"], c["n_q"], c["n_kv"], c["d"], c["norm"])
 
     def units(self):
         return self.launches * self.c["tokens"]
@@ -333,12 +363,11 @@ class GemmOp(Op):
 
     def algorithmic_bytes(self):
         c = self.c
-        return 2 * (c["m"] * c["k"] + c["n"] * c["k"] + c["n"] + c["m"] * c["n"])
+        return bytes_linear(c["m"], c["n"], c["k"])
 
     def unfused_bytes(self):
         c = self.c
-        y = c["m"] * c["n"] * 2
-        return self.algorithmic_bytes() + 2 * y + 2 * y + c["n"] * 2   # + bias add pass + GELU pass
+        return bytes_unfused_linear(c["m"], c["n"], c["k"])
 
     def units(self):
         return self.c["m"]
@@ -432,8 +461,7 @@ class FoldOp(Op):
         self.gbf.bn_fold(self.w, self.b, self.g, self.be, self.mu, self.var, self.c["eps"], self.wo, self.bo)
 
     def algorithmic_bytes(self):
-        n, k = self.c["n"], self.c["k"]
-        return 2 * n * k * 2 + 2 * n * 2 + 4 * n * 4
+        return bytes_bn_fold(self.c["n"], self.c["k"])
 
     def unfused_bytes(self):
         return self.algorithmic_bytes()
@@ -699,12 +727,12 @@ def cpu_baseline_sample(scale=1, gemm=True):
     c = workloads.config_qwen3_qkv(tokens=tq)
     dt = timed(lambda: chains.qkv_split_norm_rope(c["qkv"], 32, 8, 128, 0, c["q_w"], c["k_w"], c["eps"], 0, c["pos"],
                                                   c["theta"]))
-    res["qwen3_qkv"] = (bytes_qkv(tq, 32, 8, 128, 0, 0), dt)
+    res["qwen3_qkv"] = (bytes_qkv(tq, 32, 8, 128), dt)
     tc = 128 * scale
     c = workloads.config_chameleon_qkv(tokens=tc)
     dt = timed(lambda: chains.qkv_split_norm_rope(c["qkv"], 32, 32, 128, chains.QKNORM_LAYERNORM, c["q_w"], c["k_w"],
                                                   c["eps"], 0, c["pos"], c["theta"], q_b=c["q_b"], k_b=c["k_b"]))
-    res["chameleon_qkv_ln"] = (bytes_qkv_layernorm(tc, 32, 32, 128), dt)
+    res["chameleon_qkv_ln"] = (bytes_qkv(tc, 32, 32, 128), dt)
     ts = 16 * scale
     c = workloads.config_swiglu_ffn(rows=ts)
     dt = timed(lambda: chains.gated_act(c["x"], 11008, 3))
@@ -713,7 +741,7 @@ def cpu_baseline_sample(scale=1, gemm=True):
     c = workloads.config_wan_qkv(tokens=tw)
     dt = timed(lambda: chains.qkv_split_norm_rope(c["qkv"], 40, 40, 128, 1, c["q_w"], c["k_w"], c["eps"], 1,
                                                   c["pos"], c["theta"], sections=c["sections"]))
-    res["wan_qkv3d"] = (bytes_qkv(tw, 40, 40, 128, 1, 1), dt)
+    res["wan_qkv3d"] = (bytes_qkv(tw, 40, 40, 128), dt)
     if gemm:                       # GFLOP/s only; not part of the GB/s value
         mg = 16 * scale
         c = workloads.linear_gelu_case(mg, 16384, 4096, seed=0)
@@ -737,7 +765,7 @@ def cpu_baseline_sample(scale=1, gemm=True):
     ch = 1024 * scale
     c = workloads.linear_gelu_case(1, ch, 4096, seed=0)
     dt = timed(lambda: chains.bn_fold_bf16(c["w"], c["bias"], c["gamma"], c["beta"], c["mean"], c["var"], c["eps"]))
-    res["bn_fold"] = (2 * ch * 4096 * 2 + 2 * ch * 2 + 4 * ch * 4, dt)
+    res["bn_fold"] = (bytes_bn_fold(ch, 4096), dt)
     for k, (b, dt) in res.items():
         if k not in ("linear_bias_gelu", "linear_fp8_gelu"):
             t_total += dt
@@ -893,36 +921,61 @@ def main_gpu(args):
     if status != gbf.OK:
         raise RuntimeError(f"device status after warm-up: {msg}")
 
-    barrier(pg)
-    torch.cuda.synchronize()
-    clocks.mark()
-    t_wall0 = time.perf_counter()
-    recs = []
-    for _ in range(args.steps):
-        one_step(recs)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t_wall0
-    barrier(pg)
+    # The K-step timed region runs `repeats` times back to back (each bracketed
+    # by a barrier and a device synchronisation); per operator the mean over a
+    # region's K steps is taken, and the median over the regions is reported
+    # with the spread (FlashRT §5: re-measure before accepting a number).
+    regions = []
+    walls = []
+    for rep in range(args.repeats):
+        barrier(pg)
+        torch.cuda.synchronize()
+        if rep == 0:
+            clocks.mark()
+        t_wall0 = time.perf_counter()
+        recs = []
+        for _ in range(args.steps):
+            one_step(recs)
+        torch.cuda.synchronize()
+        walls.append(time.perf_counter() - t_wall0)
+        barrier(pg)
+        per_region = {}
+        for op, e0, e1 in recs:
+            per_region.setdefault(op.name, []).append(e0.elapsed_time(e1))
+        regions.append(per_region)
     clk = clocks.stop()
 
-    per_op = {}
-    for op, e0, e1 in recs:
-        per_op.setdefault(op.name, {"op": op, "ms": []})["ms"].append(e0.elapsed_time(e1))
+    per_op = {op.name: {"op": op} for op in ops}
+    region_mem = []                      # (bytes, ms) of the memory-bound rows, per region
+    for per_region in regions:
+        b = m = 0.0
+        for name, ts in per_region.items():
+            op = per_op[name]["op"]
+            per_op[name].setdefault("region_ms", []).append(sum(ts) / len(ts))
+            per_op[name].setdefault("all_ms", []).extend(ts)
+            if op.bound != "tensor":
+                b += op.algorithmic_bytes()
+                m += sum(ts) / len(ts)
+        region_mem.append((b, m))
 
     mem_bytes = mem_ms = 0.0
     step_ms = 0.0
     out_ops = {}
     for name, d in per_op.items():
         op = d["op"]
-        ms = sum(d["ms"]) / len(d["ms"])       # the mean: whole-job time over the timed steps
+        ms = statistics.median(d["region_ms"])   # median over the regions of each region's mean
         step_ms += ms
-        entry = {"ms": round(ms, 5), "ms_median": round(statistics.median(d["ms"]), 5), "launches": op.launches,
+        entry = {"ms": round(ms, 5), "ms_median": round(statistics.median(d["all_ms"]), 5),
+                 "ms_regions": [round(x, 5) for x in d["region_ms"]],
+                 "spread": round((max(d["region_ms"]) - min(d["region_ms"])) / ms, 4), "launches": op.launches,
                  "tokens_per_s": round(op.units() / (ms / 1e3), 1)}
         if op.bound == "tensor":
             tf = op.flops() / (ms / 1e3) / 1e12
-            peak = peaks["bf16_tflops"] * getattr(op, "peak_ratio", 1.0)
+            ratio = getattr(op, "peak_ratio", 1.0)
+            peak = peaks["bf16_tflops"] * ratio
             entry.update({"tflops": round(tf, 1), "frac_of_peak": round(tf / peak, 4), "peak_tflops": round(peak, 1),
-                          "bytes": op.algorithmic_bytes()})
+                          "frac_of_nominal": round(tf / (BF16_DENSE_NOMINAL_TFLOPS * ratio), 4),
+                          "bytes": op.algorithmic_bytes(), "unfused_bytes": op.unfused_bytes()})
         else:
             gbs = op.algorithmic_bytes() / (ms / 1e3) / 1e9
             entry.update({"gbs": round(gbs, 1), "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4),
@@ -931,11 +984,13 @@ def main_gpu(args):
             mem_ms += ms
         out_ops[name] = entry
 
-    # timing is the slowest rank; value sums the bytes all ranks moved
-    mem_ms_max = max_over_ranks(pg, mem_ms)
+    # value: the median region's aggregate; timing is the slowest rank, bytes sum over ranks
+    region_vals = []
+    for b, m in region_mem:
+        m_max = max_over_ranks(pg, m)
+        region_vals.append(sum_over_ranks(pg, b) / (m_max / 1e3) / 1e9 if m_max > 0 else 0.0)
+    value = statistics.median(region_vals)
     step_ms_max = max_over_ranks(pg, step_ms)
-    total_bytes = sum_over_ranks(pg, mem_bytes)
-    value = total_bytes / (mem_ms_max / 1e3) / 1e9 if mem_ms_max > 0 else 0.0
 
     # roofline: the memory-bound kernel with the largest share of the step among
     # those whose launch moves more than L2 holds (HBM-bound by construction);
@@ -957,25 +1012,33 @@ def main_gpu(args):
             "data": "synthetic (seeded numpy PCG64, the workloads' shapes and distributions)",
             "config": {"workload": "fused hot path: " + ", ".join(per_op), "parallelism": f"replicas x{world}",
                        "l2": "flushed (512 MB write, then read back) before every operator, outside its event pair",
-                       "value_scope": "memory-bound fused kernels; GEMM timed in the same step, see ops"},
+                       "value_scope": "memory-bound fused kernels; GEMM timed in the same step, see ops",
+                       "repeats": f"the {args.steps}-step timed region ran {args.repeats} times; per operator the "
+                                  "median of the regions' means, spread = (max - min) / median"},
+            "repeats": args.repeats, "value_regions": [round(v, 1) for v in region_vals],
             "roofline": roofline, "ops": out_ops, "clocks": clk,
             "peaks": {"hbm_gbs_measured_copy": peaks["hbm_gbs"], "bf16_tflops_measured": peaks["bf16_tflops"],
-                      "source": peaks["source"], "hbm_gbs_nominal": 7900.0, "bf16_tflops_dense_nominal": 2250.0,
+                      "bf16_tflops_measured_sustained": peaks["bf16_tflops_sustained"],
+                      "source": peaks["source"], "hbm_gbs_nominal": 7900.0,
+                      "bf16_tflops_dense_nominal": BF16_DENSE_NOMINAL_TFLOPS,
                       "nominal_source": "GB300 nominal figures (HBM3e 7.9 TB/s; dense bf16 2.25 PFLOP/s)",
                       "gbf_copy_gbs": copy_probe_gbs(gbf)},
             "latency_bound": {n: {"us_per_launch": round(d["ms"] * 1e3 / d["launches"], 3), "launches": d["launches"]}
                               for n, d in out_ops.items()
                               if "gbs" in d and per_op[n]["op"].algorithmic_bytes() // per_op[n]["op"].launches < (1 << 20)},
             "gpu_launches": args.steps * sum(op.launches for op in ops),
-            "wall_s_timed_region": round(wall, 3)}
+            "wall_s_timed_region": round(statistics.median(walls), 3)}
     if with_gemm and "linear_bias_gelu" in out_ops:
         g = out_ops["linear_bias_gelu"]
-        gop = per_op["linear_bias_gelu"]["op"]
         line["roofline_gemm"] = {"kernel": "linear_bias_gelu", "bound": "tensor", "achieved": g["tflops"],
                                  "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                  "frac": round(g["tflops"] / peaks["bf16_tflops"], 4),
+                                 "frac_of_nominal": g["frac_of_nominal"],
                                  "peak_source": f"{peaks['source']} (burst cuBLAS bf16)",
                                  "traffic": kernel_traffic("linear_bias_gelu")}
+        if args.gemm_sustained_s > 0:
+            line["roofline_gemm"]["sustained"] = gemm_sustained(per_op["linear_bias_gelu"]["op"], local, peaks,
+                                                                args.gemm_sustained_s)
 
     # end to end through the C ABI with host buffers: H2D inputs, op, D2H outputs
     if not args.no_e2e:
@@ -989,6 +1052,40 @@ def main_gpu(args):
         print(json.dumps(line))
     if pg is not None:
         pg.destroy_process_group()
+
+
+def gemm_sustained(op, cuda_index, peaks, seconds):
+    """The GEMM launched back to back for about `seconds` on its operands (no
+    L2 flush between launches: X and W stay partly resident, as they would in
+    a model's repeated layer), timed with events around the whole run, with
+    the SM clock and power sampled during it.  Reported against the measured
+    sustained bf16 peak (a seconds-long cuBLAS loop under the power cap) and as
+    time x median SM MHz, which takes the clock out of the comparison."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    op.run()
+    e1.record()
+    torch.cuda.synchronize()
+    n = max(10, int(seconds * 1e3 / max(e0.elapsed_time(e1), 1e-3)))
+    clocks = ClockSampler(cuda_index)
+    clocks.start()
+    clocks.mark()
+    e0.record()
+    for _ in range(n):
+        op.run()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / n
+    tf = op.flops() / (ms / 1e3) / 1e12
+    sus = peaks.get("bf16_tflops_sustained")
+    out = {"launches": n, "seconds": round(e0.elapsed_time(e1) / 1e3, 2), "ms_per_launch": round(ms, 5),
+           "tflops": round(tf, 1), "peak": sus, "frac": round(tf / sus, 4) if sus else None,
+           "frac_of_nominal": round(tf / BF16_DENSE_NOMINAL_TFLOPS, 4), "clocks": clk}
+    if clk.get("sm_mhz"):
+        out["ms_x_mhz"] = round(ms * clk["sm_mhz"], 1)
+    return out
 
 
 def measure_e2e(ops, args, stream):
@@ -1121,6 +1218,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--repeats", type=int, default=3, help="times the K-step timed region runs (median reported)")
+    ap.add_argument("--gemm-sustained-s", type=float, default=3.0,
+                    help="seconds of back-to-back GEMM launches for the sustained figure (0: skip)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-gemm", action="store_true", help="leave the GEMM row out of the step")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
