@@ -68,9 +68,14 @@ def quant_e4m3_static(y, s_q):
 
     The scale is a descale: code = e4m3(y / s_q), dequantised value = code * s_q.
     s_q crosses the C boundary as a binary32, so its binary32 value is used.
-    y / s_q is formed in float64 and rounded once to binary32, the precision in
-    which the kernel takes the same rounding decision; the E4M3 encoder then
-    saturates to +-448 and rounds to nearest even."""
+    y / s_q is formed in float64 and rounded once to binary32; the E4M3 encoder
+    then saturates to +-448 and rounds that binary32 value to nearest even.
+    The binary32 step follows the pages' precision rule for fused kernels: the
+    intermediate is held in an FP32 register and converted to the storage type
+    once, at the write (OpenPPL §6.2: FP32 accumulators, converted only on the
+    write-back; HowTo §4.1: keep the FP32 accumulator and convert once before
+    writing).  The two readings differ only within half a binary32 ulp of an
+    E4M3 midpoint."""
     s = np.float64(np.float32(s_q))
     v = (np.asarray(y, np.float64) / s).astype(np.float32)
     return e4m3_encode_sat(v)

@@ -413,3 +413,34 @@ def test_bn_fold_fp32_is_one_ieee_op_per_step():
     s = r32(d(gamma) / r32(np.sqrt(r32(d(var) + d(eps)))))
     assert np.array_equal(wf, r32(d(w) * s[:, None]).astype(np.float32))
     assert np.array_equal(bf, r32(r32(r32(d(b) - d(mean)) * s) + d(beta)).astype(np.float32))
+
+
+# ------------------------------------------------------- static E4M3 quantiser
+
+def test_quantiser_rounds_y_over_s_to_binary32_before_the_e4m3_decision():
+    """The quantiser's input is the FP32 value a fused kernel holds (OpenPPL
+    §6.2, HowTo §4.1: FP32 in registers, one conversion at the write).  Values
+    placed within half a binary32 ulp (2**-24 at 1.0) of an E4M3 midpoint tell
+    that reading from rounding the float64 y / s directly: 1.0625 + 2**-30 is a
+    binary32 tie between 1.0 (code 0x38, even fraction) and 1.125 (0x39), so it
+    goes to 0x38, while the float64 value lies above the midpoint (0x39);
+    1.1875 - 2**-30 ties between 1.125 (0x39) and 1.25 (0x3A, even) and goes to
+    0x3A, while the float64 value lies below (0x39).  With the descale 0.5
+    (binary32-exact) the same values, halved, give the same codes; negated,
+    the codes gain the sign bit."""
+    y = np.array([1.0625 + 2.0 ** -30, 1.1875 - 2.0 ** -30])
+    assert ops.quant_e4m3_static(y, 1.0).tolist() == [0x38, 0x3A]
+    assert ops.quant_e4m3_static(y / 2, 0.5).tolist() == [0x38, 0x3A]
+    assert ops.quant_e4m3_static(-y, 1.0).tolist() == [0xB8, 0xBA]
+    # away from a midpoint the two readings agree: 1.0625 + 2**-20 is above the tie in binary32 too
+    assert ops.quant_e4m3_static(np.array([1.0625 + 2.0 ** -20]), 1.0).tolist() == [0x39]
+
+
+def test_quantiser_uses_the_binary32_descale():
+    """s crosses the C boundary as a binary32: 0.05 is 0.0500000007..., so
+    y = 0.05 * 448 in float64 lands just under 448 after the division and is
+    still the largest code; y / s for a y past 448 s saturates (0x7E / 0xFE)."""
+    s32 = float(np.float32(0.05))
+    assert s32 != 0.05
+    assert ops.quant_e4m3_static(np.array([448 * 0.05, 1e3, -1e3]), 0.05).tolist() == [0x7E, 0x7E, 0xFE]
+    assert ops.quant_e4m3_static(np.array([448 * s32 * (1 + 2.0 ** -20)]), 0.05).tolist() == [0x7E]
