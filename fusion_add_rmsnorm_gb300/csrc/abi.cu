@@ -300,8 +300,11 @@ int linear_entry(const char* fn, bool fp8, const void* X, float x_scale, const v
   if (K % kq != 0 || N % 16 != 0)
     return fail(GBF_EUNSUPPORTED, "%s: needs K %% %lld == 0 and N %% 16 == 0 (K=%lld, N=%lld)", fn, (long long)kq,
                 (long long)K, (long long)N);
-  if (M > (1LL << 31) || N > (1LL << 31) || K > (1LL << 31))
-    return fail(GBF_EUNSUPPORTED, "%s: extents must be below 2^31", fn);
+  // the kernel indexes rows, columns, tile counts and TMA coordinates with int32
+  const int64_t lim = 1LL << 31;
+  if (M >= lim || N >= lim || K >= lim) return fail(GBF_EUNSUPPORTED, "%s: M, N and K must be below 2^31", fn);
+  if (((M + 127) / 128) * ((N + 255) / 256) >= lim)
+    return fail(GBF_EUNSUPPORTED, "%s: more than 2^31 - 1 output tiles of 128 x 256", fn);
   if (M == 0) return ok();
   if (!X || !W || !Y || (fp8 && !w_scale)) return fail(GBF_EINVAL, "%s: X, W, Y (and w_scale) are required", fn);
   if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || (bias && !aligned16(bias)) ||

@@ -187,6 +187,11 @@ def test_linear_and_fold_and_copy_validation(gbf):
     assert lin(x=None) == gbf.EINVAL
     assert lin(y=ctypes.c_void_p(4 * F + 2)) == gbf.EALIGN
     assert lin(y=A(0)) == gbf.EINVAL
+    # int32 extents inside the kernel: 2^31 itself is refused, as is a tile count past 2^31 - 1
+    assert lin(m=1 << 31) == gbf.EUNSUPPORTED
+    assert lin(n=1 << 31) == gbf.EUNSUPPORTED
+    assert lin(k=1 << 31) == gbf.EUNSUPPORTED
+    assert lin(m=(1 << 31) - 1, n=(1 << 31) - 16) == gbf.EUNSUPPORTED
     fold = lambda **k: L.gbf_bn_fold(*[k.get(n, d) for n, d in [                   # noqa: E731
         ("w", A(0)), ("b", None), ("g", A(1)), ("be", A(2)), ("mu", A(3)), ("var", A(4)), ("eps", 1e-2),
         ("oc", 8), ("inner", 27), ("wo", A(5)), ("bo", A(6)), ("s", None)]])
