@@ -145,3 +145,71 @@ def test_fused_codes_at_least_as_close_as_the_unfused_chain(gbf, mode):
         d = formats.e4m3_decode(codes).astype(np.float64).ravel()
         return float(d @ y / np.linalg.norm(d) / np.linalg.norm(y))
     assert cos(q) >= cos(q_unfused) - 1e-9, (cos(q), cos(q_unfused))
+
+
+# ------------------------------------------------------------ E4M3 range edges
+# The quantiser saturates to +-448 instead of producing NaN (OpenPPL §6.4: a
+# fused clamp has to see the quantisation scale; FlashRT §2.1 / §3: the fused
+# kernel writes FP8 codes for the next layer).  These cases drive the kernel to
+# both ends of the E4M3 range in every mode, with and without the gate, in the
+# one-vector launch plan ([16, 256]), the two-vector plan of the bench
+# ([65536, 4096]) and the four-vector plan ([2003, 8192]).
+
+E4M3_NAN_CODES = (0x7F, 0xFF)
+
+
+def check_edge(gbf, c, rows=None, what=""):
+    res_out, q = run_gpu(gbf, c)
+    ref_res, ref_q = run_oracle(c, rows)
+    if rows is not None:
+        res_out, q = res_out[rows], q[rows]
+    assert_bf16_close(res_out, ref_res, what + " res_out")
+    assert_fp8_codes(q, ref_q, what + " q")
+    assert not np.isin(q, E4M3_NAN_CODES).any(), f"{what}: NaN code written"
+    kind = c["kind"]
+    if kind == "saturate":
+        sat = np.isin(q, (0x7E, 0xFE))
+        assert sat.mean() > 0.2, f"{what}: only {sat.mean():.3f} of codes saturated"
+        assert (q == 0x7E).any() and (q == 0xFE).any(), f"{what}: saturation not reached on both signs"
+    elif kind == "subnormal":
+        mag = q & 0x7F
+        assert (mag < 0x08).mean() > 0.5, f"{what}: only {(mag < 0x08).mean():.3f} of codes subnormal or zero"
+        assert ((mag > 0) & (mag < 0x08)).any() and (mag == 0).any(), what
+    elif kind == "outlier" and q.shape[-1] >= 1024:
+        # the outlier's normalised value is about sqrt(hidden) >= 32, past 448 * 0.05 (a gate near zero can
+        # take a row's outlier back into range)
+        rowsat = np.isin(q, (0x7E, 0xFE)).any(axis=1).mean()
+        assert rowsat > 0.9, f"{what}: only {rowsat:.3f} of the outlier rows saturated"
+    return q
+
+
+@pytest.mark.parametrize("kind", workloads.EDGE_KINDS)
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("gated", [False, True])
+def test_e4m3_range_edges_one_vector_plan(gbf, kind, mode, gated):
+    c = workloads.add_rmsnorm_edge_case(16, 256, mode, kind, seed=40 + mode, gated=gated)
+    q = check_edge(gbf, c, what=f"[16,256] {kind} mode {mode} gated {gated}")
+    if kind == "zero_rows" and mode != 2:
+        # a zero residual row normalises to zero: every code is +0 or -0 (row 1 sums to zero without a gate)
+        assert np.isin(q[::3], (0x00, 0x80)).all()
+        assert gated or np.isin(q[1], (0x00, 0x80)).all()
+
+
+@pytest.mark.parametrize("kind", workloads.EDGE_KINDS)
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_e4m3_range_edges_bench_plan(gbf, kind, mode):
+    """65536 x 4096 in the bench's launch configuration; the oracle checks the
+    first rows (rows 0 and 1 are the zero rows of that kind), the last row and
+    60 random rows."""
+    c = workloads.add_rmsnorm_edge_case(65536, 4096, mode, kind, seed=60 + mode, gated=mode == 2)
+    rng = np.random.default_rng(workloads.EDGE_KINDS.index(kind))
+    pick = np.unique(np.concatenate([[0, 1, 2, 3, 65535], rng.choice(65536, 60, replace=False)]))
+    check_edge(gbf, c, rows=pick, what=f"65536x4096 {kind} mode {mode}")
+
+
+@pytest.mark.parametrize("kind", ["saturate", "outlier"])
+@pytest.mark.parametrize("mode", [0, 2])
+def test_e4m3_range_edges_four_vector_plan(gbf, kind, mode):
+    c = workloads.add_rmsnorm_edge_case(2003, 8192, mode, kind, seed=80 + mode, gated=mode == 2)
+    pick = np.unique(np.concatenate([[0, 1, 2002], np.random.default_rng(mode).choice(2003, 40, replace=False)]))
+    check_edge(gbf, c, rows=pick, what=f"[2003,8192] {kind} mode {mode}")

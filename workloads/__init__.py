@@ -64,6 +64,47 @@ def add_rmsnorm_case(rows, hidden, mode, seed=0, gated=False):
     return c
 
 
+EDGE_KINDS = ("saturate", "subnormal", "zero_rows", "outlier")
+
+
+def add_rmsnorm_edge_case(rows, hidden, mode, kind, seed=0, gated=False):
+    """add_rmsnorm_case with inputs that reach the ends of the E4M3 range.
+
+    kind "saturate":  the descale is 0.002 instead of 0.05, so every |y| above
+                      0.896 lies past the largest finite code (448 * 0.002);
+    kind "subnormal": the descale is 200, so |y / s| of a unit-RMS row mostly
+                      falls below 2**-6, among the E4M3 subnormals and zeros;
+    kind "zero_rows": every third row of x and res is all zeros, and in row 1
+                      (when there is one) x is res with every sign bit flipped,
+                      so the residual sum is exactly zero there too;
+    kind "outlier":   one column of every row of x holds a value of magnitude
+                      10**U(3, 6) with a random sign; the norm's scale is then
+                      set by that one value and the other columns land near
+                      the bottom of the E4M3 range, while the outlier saturates.
+    The other draws are those of add_rmsnorm_case with the same seed; the
+    extra draws (outlier columns, magnitudes, signs) come after them."""
+    if kind not in EDGE_KINDS:
+        raise ValueError(kind)
+    c = add_rmsnorm_case(rows, hidden, mode, seed=seed, gated=gated)
+    c["kind"] = kind
+    if kind == "saturate":
+        c["s_q"] = 0.002
+    elif kind == "subnormal":
+        c["s_q"] = 200.0
+    elif kind == "zero_rows":
+        c["x"][::3] = 0
+        c["res"][::3] = 0
+        if rows > 1:
+            c["x"][1] = c["res"][1] ^ np.uint16(0x8000)
+    else:
+        d = Draw(seed + 7919)
+        col = d.rng.integers(0, hidden, size=rows)
+        mag = np.power(np.float32(10.0), d.uniform((rows,), 3.0, 6.0))
+        sign = np.where(d.rng.random(rows) < 0.5, np.float32(-1.0), np.float32(1.0))
+        c["x"][np.arange(rows), col] = _bf16_bits(mag * sign)
+    return c
+
+
 def config_tiny_add_rmsnorm(seed=0):
     """Residual + RMSNorm + FP8: x, res bf16 [16, 256] ~ N(0,1), weight
     1 + N(0, 0.1) [256], eps 1e-6, static scale 0.05."""
@@ -210,3 +251,17 @@ def norm_fold_case(out_ch, inner, seed=0):
     d = Draw(seed)
     return {"w": d.bf16_normal((out_ch, inner), std=0.02), "gamma": d.bf16_normal((inner,), std=0.1),
             "out_ch": out_ch, "inner": inner}
+
+
+def cross_layer_case(rows, hidden, n_out, seed=0):
+    """The loop between two layers: x, res ~ N(0,1) [rows, hidden] into the
+    _noweight norm, a Gemma-style norm weight gamma ~ N(0, 0.1) [hidden] (the
+    scale is 1 + gamma), the next Linear's W ~ N(0, 0.02) [n_out, hidden] and
+    bias ~ N(0, 0.1) [n_out] (bf16 bits), one weight descale per output row ~
+    U(0.9, 1.1) * 0.1 / 448 (float32), activation descale 0.05, eps 1e-6."""
+    d = Draw(seed)
+    return {"x": d.bf16_normal((rows, hidden)), "res": d.bf16_normal((rows, hidden)),
+            "gamma": d.bf16_normal((hidden,), std=0.1), "w": d.bf16_normal((n_out, hidden), std=0.02),
+            "bias": d.bf16_normal((n_out,), std=0.1),
+            "w_scale": (d.uniform((n_out,), 0.9, 1.1) * (0.1 / 448.0)).astype(np.float32),
+            "x_scale": 0.05, "eps": 1e-6, "rows": rows, "hidden": hidden, "n_out": n_out}
