@@ -12,9 +12,12 @@
 // A group of TPR threads (a power of two, 8..512) owns one row; each thread
 // owns NV vectors strided by TPR, so one warp instruction touches TPR*16
 // contiguous bytes.  CTAs are persistent: a CTA walks rows with a grid-sized
-// stride, keeps its columns' weight factors in registers for the whole launch,
-// and loads the next row's x and res while it reduces and writes the current
-// one.
+// stride, keeps its columns' factors (weight, gate, AdaRMSNorm scale and shift)
+// in registers or, where registers would cost resident CTAs, in shared memory
+// for the whole launch, and (up to four vectors per thread) loads the next
+// row's x and res while it reduces and writes the current one.  A row wider
+// than one warp reduces through per-warp partial sums in shared memory with
+// one barrier per row.
 //
 // Rounding points: res_out = bf16(x + res) or bf16(res + gate * x), one
 // rounding of the exact value (bf16x2 add / fused multiply-add); the norm reads
@@ -23,6 +26,7 @@
 // code = e4m3_rne_sat(y / s).
 #include <map>
 #include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -30,10 +34,22 @@
 namespace gbf {
 namespace {
 
+// Where a thread keeps the per-column factors (weight, gate, AdaRMSNorm scale
+// and shift) of its NV vectors:
+//  kFacReg   float32 in registers with the descale folded in (one or two
+//            vectors per thread, no AdaRMSNorm at two);
+//  kFacPack  packed bf16 in registers, widened at each use (the launch-bound
+//            warp-per-row plan: every factor requested with the row);
+//  kFacSmem  packed bf16 in shared memory, copied there once per CTA (wide
+//            rows and AdaRMSNorm at two vectors, where registers would cost
+//            resident CTAs).
+enum { kFacReg = 0, kFacPack = 1, kFacSmem = 2 };
+
 constexpr int kMaxBlock = 512;
-// Threads per CTA of the NV-vector kernel: rows of two vectors per thread use
-// at most 256 threads, so three CTAs fit on an SM.
-constexpr int max_block(int nv) { return nv == 2 ? 256 : kMaxBlock; }
+constexpr int max_block(int nv) { return nv == 1 || nv == 8 ? kMaxBlock : 256; }
+// resident CTAs the register budget is sized for: three of 256 threads at two
+// vectors, two at four (each with the next row in flight)
+constexpr int min_blocks(int nv, int fac) { return fac == kFacPack ? 1 : nv == 2 ? 3 : nv == 4 ? 2 : 1; }
 
 GBF_DEVICE uint4 bf16x8_add(uint4 a, uint4 b) {
   uint4 r;
@@ -57,17 +73,41 @@ GBF_DEVICE uint4 bf16x8_fma(uint4 g, uint4 x, uint4 r0) {
   return r;
 }
 
-template <int MODE, bool GATED, int NV>
-__global__ void __launch_bounds__(max_block(NV), NV == 2 ? 3 : 1)
+// Factor vectors per column group: the gate (GATED) first, then the weight
+// (WEIGHT) or the scale and the shift (ADA).
+template <int MODE, bool GATED>
+constexpr int factor_count() { return (GATED ? 1 : 0) + (MODE == kNormWeight ? 1 : 0) + (MODE == kNormAda ? 2 : 0); }
+
+// Per-column factors from packed bf16 with the descale folded in:
+//   WEIGHT: fa = w / s;  ADA: fa = (1 + scale) / s, fb = shift / s.
+template <int MODE>
+GBF_DEVICE void unpack_factors(uint4 f0, uint4 f1, float rs, float (&fa)[8], float (&fb)[8]) {
+  if (MODE == kNormWeight) {
+    float w[8];
+    bf16x8_to_f32(f0, w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) fa[i] = w[i] * rs;
+  } else if (MODE == kNormAda) {
+    float sc[8], sh[8];
+    bf16x8_to_f32(f0, sc);
+    bf16x8_to_f32(f1, sh);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      fa[i] = (1.0f + sc[i]) * rs;
+      fb[i] = sh[i] * rs;
+    }
+  }
+}
+
+template <int MODE, bool GATED, int NV, int FAC>
+__global__ void __launch_bounds__(max_block(NV), min_blocks(NV, FAC))
 add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
-  // Rows of up to 2 vectors per thread keep the next row's inputs in
-  // registers (prefetch); wider rows (BIG) issue their loads at the top of
-  // each row.  The per-column factors stay in registers (REGF) for 1 vector
-  // per thread, and for 2 unless the mode is AdaRMSNorm (two factor vectors
-  // plus the gate); otherwise they are reloaded from L1 every row, which keeps
-  // three CTAs per SM.
-  constexpr bool BIG = NV > 2;
-  constexpr bool REGF = NV == 1 || (NV == 2 && MODE != kNormAda);
+  // Rows of up to four vectors per thread keep the next row's x and res in
+  // registers (prefetch); wider rows issue their loads at the top of each row.
+  constexpr bool PF = NV <= 4;
+  constexpr int NFAC = factor_count<MODE, GATED>();
+  constexpr int NREG = FAC == kFacReg ? NV : 1;     // float factor sets held in registers
+  constexpr int NPK = FAC == kFacPack ? NV : 1;     // packed factor sets held in registers
   const int tpr = a.tpr;
   const int lane = threadIdx.x & (tpr - 1);
   const int row_in_cta = threadIdx.x / tpr;
@@ -78,44 +118,16 @@ add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
   __nv_bfloat16* res_out = static_cast<__nv_bfloat16*>(a.res_out);
   uint8_t* q_out = static_cast<uint8_t*>(a.q_out);
   const float rs = 1.0f / a.fp8_scale;
+  // factor sources in the order of factor_count: gate, weight | scale, shift
+  const void* fsrc[3] = {GATED ? a.gate : (MODE == kNormWeight ? a.weight : a.ada_scale),
+                         GATED ? (MODE == kNormWeight ? a.weight : a.ada_scale) : a.ada_shift, a.ada_shift};
+  extern __shared__ uint4 sfac[];                   // kFacSmem: [NFAC][nvec] packed bf16
 
   pdl_wait();
 
   bool vok[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k) vok[k] = lane + k * tpr < nvec;
-
-  // Per-column factors (descale folded in):
-  //   WEIGHT: fa = w / s;  NOWEIGHT: none;  ADA: fa = (1 + scale) / s, fb = shift / s.
-  auto factors = [&](int k, float* fa, float* fb) {
-    const int col = (lane + k * tpr) * 8;
-    if (MODE == kNormWeight) {
-      float w[8];
-      bf16x8_to_f32(ld_cached(static_cast<const __nv_bfloat16*>(a.weight) + col), w);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) fa[i] = w[i] * rs;
-    } else if (MODE == kNormAda) {
-      float sc[8], sh[8];
-      bf16x8_to_f32(ld_cached(static_cast<const __nv_bfloat16*>(a.ada_scale) + col), sc);
-      bf16x8_to_f32(ld_cached(static_cast<const __nv_bfloat16*>(a.ada_shift) + col), sh);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        fa[i] = (1.0f + sc[i]) * rs;
-        fb[i] = sh[i] * rs;
-      }
-    }
-  };
-  constexpr int NF = REGF ? NV : 1;
-  float fa[NF][8], fb[NF][8];
-  uint4 gate[NF];
-  if (REGF) {
-#pragma unroll
-    for (int k = 0; k < NF; ++k) {
-      if (!vok[k]) continue;
-      if (GATED) gate[k] = ld_cached(static_cast<const __nv_bfloat16*>(a.gate) + (lane + k * tpr) * 8);
-      factors(k, fa[k], fb[k]);
-    }
-  }
 
   int64_t row = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta + row_in_cta;
   uint4 xr[NV], rr[NV];
@@ -130,10 +142,65 @@ add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
         }
     }
   };
-  if (!BIG) load_row(row);
+  if (PF) load_row(row);
+  // the factors are requested after the first row, whose loads need nothing
+  float fa[NREG][8], fb[NREG][8];
+  uint4 gate[NREG];
+  uint4 pk[NPK][NFAC > 0 ? NFAC : 1];
+  if (FAC == kFacReg) {
+#pragma unroll
+    for (int k = 0; k < NREG; ++k) {
+      if (!vok[k]) continue;
+      const int c = lane + k * tpr;
+      uint4 f[3] = {};
+#pragma unroll
+      for (int j = 0; j < NFAC; ++j) f[j] = ld_cached(static_cast<const uint4*>(fsrc[j]) + c);
+      if (GATED) gate[k] = f[0];
+      unpack_factors<MODE>(f[GATED ? 1 : 0], f[GATED ? 2 : 1], rs, fa[k], fb[k]);
+    }
+  } else if (FAC == kFacPack) {
+#pragma unroll
+    for (int k = 0; k < NPK; ++k)
+      if (vok[k])
+#pragma unroll
+        for (int j = 0; j < NFAC; ++j) pk[k][j] = ld_cached(static_cast<const uint4*>(fsrc[j]) + lane + k * tpr);
+  }
+
+  if (FAC == kFacSmem && NFAC > 0) {
+    // the copy's loads are issued in batches of about eight per thread, so a
+    // CTA waits about one round trip per batch, not one per vector
+    constexpr int kStageBatch = NFAC >= 3 ? 2 : 8 / (NFAC > 0 ? NFAC : 1);
+    for (int i0 = threadIdx.x; i0 < nvec; i0 += kStageBatch * blockDim.x) {
+      uint4 f[NFAC > 0 ? NFAC : 1][kStageBatch];
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int i = i0 + u * blockDim.x;
+#pragma unroll
+        for (int j = 0; j < NFAC; ++j)
+          if (i < nvec) f[j][u] = ld_cached(static_cast<const uint4*>(fsrc[j]) + i);
+      }
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int i = i0 + u * blockDim.x;
+#pragma unroll
+        for (int j = 0; j < NFAC; ++j)
+          if (i < nvec) sfac[j * nvec + i] = f[j][u];
+      }
+    }
+    __syncthreads();
+  }
   pdl_launch_dependents();
 
-  __shared__ float part[kMaxBlock / 32];
+  // Packed factors of vector k (gate first): from registers or shared memory.
+  auto packed = [&](int k, int j) -> uint4 {
+    if (FAC == kFacPack) return pk[FAC == kFacPack ? k : 0][j];
+    return sfac[j * nvec + lane + k * tpr];
+  };
+
+  // Per-warp partial sums, double-buffered by trip parity: one barrier per
+  // row (a warp that reaches trip n + 2 has passed the barrier of trip n + 1,
+  // which every warp reaches only after reading trip n's partials).
+  __shared__ float part[2][kMaxBlock / 32];
   const int warp = threadIdx.x >> 5;
   const int wpr = tpr >> 5;                        // warps per row (when tpr > 32)
   const int first_warp = tpr > 32 ? (warp / wpr) * wpr : 0;
@@ -144,13 +211,13 @@ add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
   for (int64_t trip = 0; trip < trips; ++trip, row += row_stride) {
     const bool row_ok = row < a.rows;
     uint4 cx[NV], cr[NV];
-    if (BIG) load_row(row);
+    if (!PF) load_row(row);
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       cx[k] = xr[k];
       cr[k] = rr[k];
     }
-    if (!BIG) load_row(row + row_stride);          // next row in flight during this one
+    if (PF) load_row(row + row_stride);            // next row in flight during this one
 
     uint4 rh[NV];
     float sumsq = 0.f;
@@ -159,8 +226,7 @@ add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
       for (int k = 0; k < NV; ++k) {
         if (!vok[k]) continue;
         if (GATED) {
-          const uint4 g = REGF ? gate[REGF ? k : 0]
-                               : ld_cached(static_cast<const __nv_bfloat16*>(a.gate) + (lane + k * tpr) * 8);
+          const uint4 g = FAC == kFacReg ? gate[FAC == kFacReg ? k : 0] : packed(k, 0);
           rh[k] = bf16x8_fma(g, cx[k], cr[k]);
         } else {
           rh[k] = bf16x8_add(cx[k], cr[k]);
@@ -174,12 +240,12 @@ add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
     }
     sumsq = group_sum(sumsq, tpr < 32 ? tpr : 32);
     if (tpr > 32) {
-      if ((threadIdx.x & 31) == 0) part[warp] = sumsq;
+      float* pt = part[trip & 1];
+      if ((threadIdx.x & 31) == 0) pt[warp] = sumsq;
       __syncthreads();
       float s = 0.f;
-      for (int w = 0; w < wpr; ++w) s += part[first_warp + w];
+      for (int w = 0; w < wpr; ++w) s += pt[first_warp + w];
       sumsq = s;
-      __syncthreads();                             // part[] is rewritten next trip
     }
     if (!row_ok) continue;
     const float inv = 1.0f / sqrtf(sumsq / static_cast<float>(a.hidden) + a.eps);
@@ -188,10 +254,18 @@ add_rmsnorm_fp8_kernel(AddRmsNormArgs a) {
       if (!vok[k]) continue;
       float h[8], q[8];
       bf16x8_to_f32(rh[k], h);
-      float fbig_a[8], fbig_b[8];
-      const float* fak = REGF ? fa[REGF ? k : 0] : fbig_a;
-      const float* fbk = REGF ? fb[REGF ? k : 0] : fbig_b;
-      if (!REGF) factors(k, fbig_a, fbig_b);
+      float ua[8], ub[8];
+      const float* fak = fa[0];
+      const float* fbk = fb[0];
+      if (FAC == kFacReg) {
+        fak = fa[FAC == kFacReg ? k : 0];
+        fbk = fb[FAC == kFacReg ? k : 0];
+      } else if (MODE != kNormNoWeight) {
+        unpack_factors<MODE>(packed(k, GATED ? 1 : 0), MODE == kNormAda ? packed(k, GATED ? 2 : 1) : uint4{},
+                             rs, ua, ub);
+        fak = ua;
+        fbk = ub;
+      }
       if (MODE == kNormWeight) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) q[i] = (h[i] * inv) * fak[i];
@@ -219,29 +293,53 @@ int sm_count() {
   return n;
 }
 
-// CTAs of `kern` with `block` threads that fit on one SM (cached per kernel
-// and block size; the persistent grid is capped at that many per SM).
+// CTAs of `kern` with `block` threads and `smem` dynamic shared memory that
+// fit on one SM (cached; the persistent grid is capped at that many per SM).
+// The default dynamic shared memory limit (48 KB less the static shared
+// memory) is below some factor tables, e.g. 48 KB for three [8192] vectors,
+// so the kernel's limit is raised once to the device's opt-in maximum: the
+// attribute is only an upper bound and never has to shrink.
 template <typename K>
-int resident_per_sm(K kern, int block) {
+int resident_per_sm(K kern, int block, size_t smem) {
   static std::mutex mu;
-  static std::map<std::pair<const void*, int>, int> cache;
+  static std::map<std::tuple<const void*, int, size_t>, int> cache;
+  static std::map<const void*, bool> raised;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_pair(reinterpret_cast<const void*>(kern), block);
+  const void* fn = reinterpret_cast<const void*>(kern);
+  if (smem > 0 && !raised[fn]) {
+    int dev = 0, optin = 0;
+    cudaFuncAttributes fa = {};
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    // the opt-in maximum covers static and dynamic shared memory together
+    if (cudaFuncGetAttributes(&fa, kern) == cudaSuccess && optin > static_cast<int>(fa.sharedSizeBytes) &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - static_cast<int>(fa.sharedSizeBytes)) == cudaSuccess)
+      raised[fn] = true;
+    cudaGetLastError();
+  }
+  const auto key = std::make_tuple(fn, block, smem);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, block, 0) != cudaSuccess || occ < 1) occ = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, block, smem) != cudaSuccess || occ < 1) {
+    cudaGetLastError();
+    occ = 1;                                       // the launch itself reports a configuration that cannot run
+  }
   cache[key] = occ;
   return occ;
 }
 
-template <int MODE, bool GATED, int NV>
+template <int MODE, bool GATED, int NV, int FAC>
 cudaError_t launch_nv(const AddRmsNormArgs& a, int64_t blocks, dim3 block, cudaStream_t s, bool pdl) {
-  auto kern = add_rmsnorm_fp8_kernel<MODE, GATED, NV>;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * resident_per_sm(kern, static_cast<int>(block.x));
+  auto kern = add_rmsnorm_fp8_kernel<MODE, GATED, NV, FAC>;
+  const size_t smem = FAC == kFacSmem ? static_cast<size_t>(factor_count<MODE, GATED>()) * a.hidden * 2 : 0;
+  const int per_sm = resident_per_sm(kern, static_cast<int>(block.x), smem);
+  const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks < cap ? blocks : cap));
   cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -252,38 +350,56 @@ cudaError_t launch_nv(const AddRmsNormArgs& a, int64_t blocks, dim3 block, cudaS
 }
 
 template <int MODE, bool GATED>
-cudaError_t launch_mode(const AddRmsNormArgs& a, int nv, int64_t blocks, dim3 block, cudaStream_t s, bool pdl) {
-  switch (nv) {
-    case 1: return launch_nv<MODE, GATED, 1>(a, blocks, block, s, pdl);
-    case 2: return launch_nv<MODE, GATED, 2>(a, blocks, block, s, pdl);
-    case 4: return launch_nv<MODE, GATED, 4>(a, blocks, block, s, pdl);
-    case 8: return launch_nv<MODE, GATED, 8>(a, blocks, block, s, pdl);
+cudaError_t launch_mode(const AddRmsNormArgs& a, const AddRmsNormPlan& p, cudaStream_t s, bool pdl) {
+  const dim3 block(static_cast<unsigned>(p.block));
+  switch (p.nv * 4 + p.fac) {
+    case 1 * 4 + kFacReg: return launch_nv<MODE, GATED, 1, kFacReg>(a, p.grid, block, s, pdl);
+    case 2 * 4 + kFacReg:
+      // the planner keeps AdaRMSNorm's factors in shared memory at two vectors
+      if constexpr (MODE == kNormAda) return cudaErrorInvalidValue;
+      else return launch_nv<MODE, GATED, 2, kFacReg>(a, p.grid, block, s, pdl);
+    case 2 * 4 + kFacPack: return launch_nv<MODE, GATED, 2, kFacPack>(a, p.grid, block, s, pdl);
+    case 2 * 4 + kFacSmem: return launch_nv<MODE, GATED, 2, kFacSmem>(a, p.grid, block, s, pdl);
+    case 4 * 4 + kFacPack: return launch_nv<MODE, GATED, 4, kFacPack>(a, p.grid, block, s, pdl);
+    case 4 * 4 + kFacSmem: return launch_nv<MODE, GATED, 4, kFacSmem>(a, p.grid, block, s, pdl);
+    case 8 * 4 + kFacSmem: return launch_nv<MODE, GATED, 8, kFacSmem>(a, p.grid, block, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
-
 }  // namespace
 
-AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden) {
+AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden, int mode) {
   AddRmsNormPlan p = {};
   const int64_t nvec = hidden / 8;
-  // Vectors per thread: 1 for launch-bound shapes (the most threads per row,
-  // the shortest critical path); 2 once there are at least four vectors per
-  // thread the GPU holds at once (half the per-row reduction and loop work per
-  // element); more when a row would need more than kMaxBlock threads.  Rows
-  // keep at least 8 threads.
   const bool large = rows * nvec >= 4LL * sm_count() * 2048;
-  const int target = large ? 2 : 1;
   int nv = 1;
-  while (nv < 8 && ((nv < target && nvec >= 16 * nv) || nvec > static_cast<int64_t>(nv) * max_block(nv))) nv *= 2;
+  if (!large && nvec <= 128) {
+    // Launch-bound rows of up to 1024 values: at most 64 threads per row (two
+    // vectors each above 512 values), the factors requested with the row and
+    // kept packed in registers; measured on the 180-call Pi0.5 chain
+    // ([10, 1024]), 64 threads x 2 vectors beat 128 x 1 and 32 x 4.
+    while (nv < 2 && nvec > 64 * nv) nv *= 2;
+    p.fac = nv == 1 ? kFacReg : kFacPack;
+  } else {
+    // Vectors per thread: 1 for launch-bound shapes (the most threads per row,
+    // the shortest critical path); 2 once there are at least four vectors per
+    // thread the GPU holds at once (half the per-row reduction and loop work
+    // per element); more when a row would need more than the block's threads.
+    const int target = large ? 2 : 1;
+    while (nv < 8 && ((nv < target && nvec >= 16 * nv) || nvec > static_cast<int64_t>(nv) * max_block(nv)))
+      nv *= 2;
+    p.fac = nv == 1 || (nv == 2 && mode != kNormAda) ? kFacReg : kFacSmem;
+  }
   int tpr = 8;
   while (static_cast<int64_t>(tpr) * nv < nvec) tpr *= 2;
   p.ok = static_cast<int64_t>(tpr) * nv >= nvec && tpr <= max_block(nv);
   p.nv = nv;
   p.tpr = tpr;
-  // Small rows share a CTA of 256 threads; large rows get a CTA each.
-  p.rows_per_cta = tpr >= 256 ? 1 : 256 / tpr;
+  // Streaming launches: small rows share a CTA of 256 threads, large rows get
+  // a CTA each.  Launch-bound ones: a CTA per row (at least one warp), which
+  // spreads the few rows over as many SMs.
+  p.rows_per_cta = large ? (tpr >= 256 ? 1 : 256 / tpr) : (tpr >= 32 ? 1 : 32 / tpr);
   p.block = tpr * p.rows_per_cta;
   // CTAs needed; the launch caps the persistent grid at the CTAs that fit at once
   p.grid = rows == 0 ? 0 : (rows + p.rows_per_cta - 1) / p.rows_per_cta;
@@ -291,24 +407,21 @@ AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden) {
 }
 
 cudaError_t launch_add_rmsnorm_fp8(AddRmsNormArgs a, cudaStream_t stream, bool pdl) {
-  const AddRmsNormPlan p = plan_add_rmsnorm(a.rows, a.hidden);
+  const AddRmsNormPlan p = plan_add_rmsnorm(a.rows, a.hidden, a.mode);
   if (!p.ok) return cudaErrorInvalidValue;
   if (p.grid == 0) return cudaSuccess;
   a.tpr = p.tpr;
   a.rows_per_cta = p.rows_per_cta;
-  const int64_t blocks = p.grid;
-  const dim3 block(static_cast<unsigned>(p.block));
   const bool gated = a.gate != nullptr;
   switch (a.mode) {
     case kNormWeight:
-      return gated ? launch_mode<kNormWeight, true>(a, p.nv, blocks, block, stream, pdl)
-                   : launch_mode<kNormWeight, false>(a, p.nv, blocks, block, stream, pdl);
+      return gated ? launch_mode<kNormWeight, true>(a, p, stream, pdl)
+                   : launch_mode<kNormWeight, false>(a, p, stream, pdl);
     case kNormNoWeight:
-      return gated ? launch_mode<kNormNoWeight, true>(a, p.nv, blocks, block, stream, pdl)
-                   : launch_mode<kNormNoWeight, false>(a, p.nv, blocks, block, stream, pdl);
+      return gated ? launch_mode<kNormNoWeight, true>(a, p, stream, pdl)
+                   : launch_mode<kNormNoWeight, false>(a, p, stream, pdl);
     case kNormAda:
-      return gated ? launch_mode<kNormAda, true>(a, p.nv, blocks, block, stream, pdl)
-                   : launch_mode<kNormAda, false>(a, p.nv, blocks, block, stream, pdl);
+      return gated ? launch_mode<kNormAda, true>(a, p, stream, pdl) : launch_mode<kNormAda, false>(a, p, stream, pdl);
     default:
       return cudaErrorInvalidValue;
   }

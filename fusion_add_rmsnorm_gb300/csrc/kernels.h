@@ -34,10 +34,11 @@ struct AddRmsNormArgs {
 struct AddRmsNormPlan {
   bool ok;
   int nv, tpr, rows_per_cta, block;
+  int fac;                // where the per-column factors live (registers, packed registers, shared memory)
   int64_t grid;           // CTAs needed; the launch caps it at the CTAs that fit on the GPU at once
 };
 
-AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden);
+AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden, int mode);
 cudaError_t launch_add_rmsnorm_fp8(AddRmsNormArgs a, cudaStream_t stream, bool pdl);
 
 // --------------------------------------------- packed QKV split + norm + RoPE
