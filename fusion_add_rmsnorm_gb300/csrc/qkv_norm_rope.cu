@@ -32,9 +32,10 @@
 //    l + D/16, which contain both members of its 8 rotation pairs (j, j + D/2),
 //    so the rotation is done in registers and the head's statistics are a
 //    shuffle reduction over the head's lanes.  Each thread visits every G-th
-//    head of its token (G = 8, 16 or 32 head groups; V heads are copied),
-//    issuing a batch of loads before any arithmetic, and the token's (cos, sin)
-//    are computed once per token into a shared table.
+//    head of its token (G = 8, 16 or 32 head groups, a token's G * D/16
+//    threads at most 128; V heads are copied), issuing a batch of loads before
+//    any arithmetic, and the token's (cos, sin) are computed once per token
+//    into a shared table.
 //  * qkv_staged_kernel (everything else: full-width norm and/or 3D sections,
 //    where a rotation pair need not sit in one 16-byte vector): a persistent
 //    CTA streams its tokens' packed rows through a ring of shared-memory
@@ -722,16 +723,22 @@ cudaError_t launch_rot1d_g(const QkvArgs& a, cudaStream_t stream) {
 }
 
 // G = the smallest of 8, 16, 32 head groups that leaves a thread at most
-// kRotBatch heads, within the 256 threads a token may use.
+// kRotBatch heads, within the 128 threads a token may use: a thread with more
+// heads takes them in batches.  One token per 128-thread CTA measured faster
+// than one per 256-thread CTA with a single batch (Qwen3, 48 heads: 17.1 vs
+// 19.6 us; Chameleon, 96 heads: 32.8 vs 34.8 us): the CTAs that run alone at
+// the end of the launch are shorter.
 template <int LPH>
 cudaError_t launch_rot1d(const QkvArgs& a, cudaStream_t stream) {
   const int heads = a.n_q + 2 * a.n_kv;
-  const int gmax = kRotBlock / LPH > 32 ? 32 : kRotBlock / LPH;
+  constexpr int gmax = 128 / LPH;            // 32, 16, 8 for head_dim 64, 128, 256
   int g = 8;
   while (g < gmax && g * kRotBatch < heads) g *= 2;
-  if (g == 8) return launch_rot1d_g<LPH, 8>(a, stream);
-  if (g == 16) return launch_rot1d_g<LPH, 16>(a, stream);
-  return launch_rot1d_g<LPH, (LPH <= 8 ? 32 : 16)>(a, stream);
+  if constexpr (gmax >= 32)
+    if (g == 32) return launch_rot1d_g<LPH, 32>(a, stream);
+  if constexpr (gmax >= 16)
+    if (g == 16) return launch_rot1d_g<LPH, 16>(a, stream);
+  return launch_rot1d_g<LPH, 8>(a, stream);
 }
 
 }  // namespace
