@@ -1221,44 +1221,46 @@ def main_sweep(args):
     flush_words = flush.view(torch.int64)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(0)
-    for rows in (4096, 16384, 65536):
-        for hidden in (1024, 4096, 8192):
-            nbytes_call = bytes_add_rmsnorm(rows, hidden, 0, False)
-            nsets = max(1, min(8, -(-4 * L2_BYTES // nbytes_call)))
-            bf = dict(dtype=torch.bfloat16, device="cuda")
-            sets = []
-            for _ in range(nsets):
-                x = torch.randn(rows, hidden, generator=gen, **bf)
-                res = torch.randn(rows, hidden, generator=gen, **bf)
-                sets.append((x, res, torch.empty_like(res), torch.empty(rows, hidden, dtype=torch.uint8, device="cuda")))
-            vec = lambda m, sd: (m + sd * torch.randn(hidden, generator=gen, device="cuda")).to(torch.bfloat16)  # noqa
-            w, gate, scale, shift = vec(1.0, 0.1), vec(0.0, 0.2), vec(0.0, 0.2), vec(0.0, 0.2)
-            for name, mode, gated in (("weighted", 0, False), ("noweight", 1, False), ("ada", 2, True)):
-                def call():
-                    for x, res, out, q in sets:
-                        gbf.add_rmsnorm_fp8(x, res, out, q, mode, weight=w if mode == 0 else None,
-                                            gate=gate if gated else None, ada_scale=scale if mode == 2 else None,
-                                            ada_shift=shift if mode == 2 else None, eps=1e-6, fp8_scale=0.05)
-                ts = []
-                for it in range(args.warmup + args.steps):
-                    flush.fill_(1)
-                    flush_words.sum()
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record()
-                    call()
-                    e1.record()
-                    torch.cuda.synchronize()
-                    if it >= args.warmup:
-                        ts.append(e0.elapsed_time(e1) / nsets)
-                ms = sorted(ts)[len(ts) // 2]
-                nbytes = bytes_add_rmsnorm(rows, hidden, mode, gated)
-                gbs = nbytes / (ms / 1e3) / 1e9
-                print(json.dumps({"sweep": "add_rmsnorm_fp8", "mode": name, "rows": rows, "hidden": hidden,
-                                  "us_median": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
-                                  "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                                  "l2_flushed": True, "timed_calls": args.steps, "calls_per_event": nsets}),
-                      flush=True)
-            del sets
+    shapes = [(r, h) for r in (4096, 16384, 65536) for h in (1024, 4096, 8192)]
+    if args.sweep_shapes:
+        shapes = [tuple(int(v) for v in sh.split("x")) for sh in args.sweep_shapes.split(",")]
+    for rows, hidden in shapes:
+        nbytes_call = bytes_add_rmsnorm(rows, hidden, 0, False)
+        nsets = max(1, min(8, -(-4 * L2_BYTES // nbytes_call)))
+        bf = dict(dtype=torch.bfloat16, device="cuda")
+        sets = []
+        for _ in range(nsets):
+            x = torch.randn(rows, hidden, generator=gen, **bf)
+            res = torch.randn(rows, hidden, generator=gen, **bf)
+            sets.append((x, res, torch.empty_like(res), torch.empty(rows, hidden, dtype=torch.uint8, device="cuda")))
+        vec = lambda m, sd: (m + sd * torch.randn(hidden, generator=gen, device="cuda")).to(torch.bfloat16)  # noqa
+        w, gate, scale, shift = vec(1.0, 0.1), vec(0.0, 0.2), vec(0.0, 0.2), vec(0.0, 0.2)
+        for name, mode, gated in (("weighted", 0, False), ("noweight", 1, False), ("ada", 2, True)):
+            def call():
+                for x, res, out, q in sets:
+                    gbf.add_rmsnorm_fp8(x, res, out, q, mode, weight=w if mode == 0 else None,
+                                        gate=gate if gated else None, ada_scale=scale if mode == 2 else None,
+                                        ada_shift=shift if mode == 2 else None, eps=1e-6, fp8_scale=0.05)
+            ts = []
+            for it in range(args.warmup + args.steps):
+                flush.fill_(1)
+                flush_words.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                call()
+                e1.record()
+                torch.cuda.synchronize()
+                if it >= args.warmup:
+                    ts.append(e0.elapsed_time(e1) / nsets)
+            ms = sorted(ts)[len(ts) // 2]
+            nbytes = bytes_add_rmsnorm(rows, hidden, mode, gated)
+            gbs = nbytes / (ms / 1e3) / 1e9
+            print(json.dumps({"sweep": "add_rmsnorm_fp8", "mode": name, "rows": rows, "hidden": hidden,
+                              "us_median": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+                              "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                              "l2_flushed": True, "timed_calls": args.steps, "calls_per_event": nsets}),
+                  flush=True)
+        del sets
 
 
 def main():
@@ -1277,6 +1279,8 @@ def main():
     ap.add_argument("--small", action="store_true", help="profiling-size cases (still larger than L2)")
     ap.add_argument("--sweep", action="store_true",
                     help="add+RMSNorm+FP8 over rows {4096, 16384, 65536} x hidden {1024, 4096, 8192} x 3 modes")
+    ap.add_argument("--sweep-shapes", default="",
+                    help="with --sweep: comma-separated ROWSxHIDDEN points instead of the grid (e.g. 8192x8192)")
     ap.add_argument("--_cpu-baseline-child", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--_cpu-baseline-start", type=float, default=0.0, help=argparse.SUPPRESS)
     ap.add_argument("--_cpu-baseline-nogemm", action="store_true", help=argparse.SUPPRESS)
