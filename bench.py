@@ -1026,8 +1026,8 @@ def main_gpu(args):
             "latency_bound": {n: {"us_per_launch": round(d["ms"] * 1e3 / d["launches"], 3), "launches": d["launches"]}
                               for n, d in out_ops.items()
                               if "gbs" in d and per_op[n]["op"].algorithmic_bytes() // per_op[n]["op"].launches < (1 << 20)},
-            "gpu_launches": args.steps * sum(op.launches for op in ops),
-            "wall_s_timed_region": round(statistics.median(walls), 3)}
+            "gpu_launches": args.repeats * args.steps * sum(op.launches for op in ops),
+            "wall_s_timed_region": round(sum(walls), 3)}
     if with_gemm and "linear_bias_gelu" in out_ops:
         g = out_ops["linear_bias_gelu"]
         line["roofline_gemm"] = {"kernel": "linear_bias_gelu", "bound": "tensor", "achieved": g["tflops"],
@@ -1263,6 +1263,47 @@ def main_sweep(args):
         del sets
 
 
+def main_copy_curve(args):
+    """`--copy-curve`: the bandwidth a plain copy reaches at the sizes of the
+    step's shorter calls, timed exactly as the step times them (L2 flushed,
+    then `sets` calls on distinct buffers inside one event pair): this
+    library's copy kernel and torch's, one JSON line per point.  It shows what
+    any kernel moving that many bytes in one launch can reach, ramp-up and
+    tail included."""
+    import torch
+    import fusion_add_rmsnorm_gb300 as gbf
+    peaks = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_words = flush.view(torch.int64)
+    for mb in (12.5, 25, 50, 100, 200, 400):
+        n = int(mb * 1e6) // 16 * 16
+        for nsets in (1, 4):
+            srcs = [torch.ones(n, dtype=torch.uint8, device="cuda") for _ in range(nsets)]
+            dsts = [torch.empty_like(t) for t in srcs]
+            for impl in ("gbf_copy", "torch"):
+                ts = []
+                for it in range(args.warmup + args.steps):
+                    flush.fill_(1)
+                    flush_words.sum()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for src, dst in zip(srcs, dsts):
+                        if impl == "torch":
+                            dst.copy_(src)
+                        else:
+                            gbf.copy(src, dst)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    if it >= args.warmup:
+                        ts.append(e0.elapsed_time(e1) / nsets)
+                ms = sorted(ts)[len(ts) // 2]
+                gbs = 2 * n / (ms / 1e3) / 1e9
+                print(json.dumps({"copy_curve": impl, "bytes_moved": 2 * n, "sets": nsets,
+                                  "us_median": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                                  "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4)}), flush=True)
+            del srcs, dsts
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1279,6 +1320,8 @@ def main():
     ap.add_argument("--small", action="store_true", help="profiling-size cases (still larger than L2)")
     ap.add_argument("--sweep", action="store_true",
                     help="add+RMSNorm+FP8 over rows {4096, 16384, 65536} x hidden {1024, 4096, 8192} x 3 modes")
+    ap.add_argument("--copy-curve", action="store_true",
+                    help="plain-copy bandwidth at 25 MB..800 MB moved, timed as the step times its calls")
     ap.add_argument("--sweep-shapes", default="",
                     help="with --sweep: comma-separated ROWSxHIDDEN points instead of the grid (e.g. 8192x8192)")
     ap.add_argument("--_cpu-baseline-child", type=int, default=0, help=argparse.SUPPRESS)
@@ -1287,6 +1330,9 @@ def main():
     args = ap.parse_args()
     if args.sweep:
         main_sweep(args)
+        return
+    if args.copy_curve:
+        main_copy_curve(args)
         return
     if args._cpu_baseline_child:
         if args._cpu_baseline_start:
