@@ -51,7 +51,7 @@ def test_tiny_config_residual_rmsnorm_fp8(gbf):
 @pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("gated", [False, True])
 @pytest.mark.parametrize("rows,hidden", [(1, 8), (3, 64), (37, 256), (4, 512), (6, 768), (10, 1024), (5, 1032),
-                                         (7, 4096), (3, 8192), (2, 16384), (2, 24576), (2, 32768)])
+                                         (7, 4096), (3, 8192), (3, 8200), (2, 16384), (2, 24576), (2, 32768)])
 def test_modes_and_shapes(gbf, mode, gated, rows, hidden):
     c = workloads.add_rmsnorm_case(rows, hidden, mode, seed=rows * 7 + hidden, gated=gated)
     check(gbf, c, what=f"mode {mode} gated {gated} [{rows},{hidden}]")
@@ -108,13 +108,15 @@ def test_large_sweep_shape_sampled_rows(gbf, mode, gated):
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
-@pytest.mark.parametrize("rows,hidden", [(20011, 1024), (10007, 1032), (2003, 8192), (16411, 8192), (1001, 16384)])
+@pytest.mark.parametrize("rows,hidden", [(20011, 1024), (10007, 1032), (5000, 2056), (2003, 8192), (16411, 8192),
+                                         (4099, 8200), (1001, 16384)])
 def test_large_launch_plans_sampled_rows(gbf, mode, rows, hidden):
     """Launches large enough for the multi-vector plans: two vectors per thread
     with several rows per CTA and a ragged last CTA (1024), a vector count
     that leaves lanes idle (1032), four vectors per thread with the next row
     prefetched and the factors in shared memory (8192; 16411 rows give every
-    CTA many trips of the double-buffered reduction), and eight (16384); the
+    CTA many trips of the double-buffered reduction), and eight (16384); 2056
+    and 8200 leave most of the last vector slot of every thread idle; the
     oracle checks the first, last and 62 random rows."""
     c = workloads.add_rmsnorm_case(rows, hidden, mode, seed=rows + hidden + mode, gated=mode == 2)
     pick = np.unique(np.concatenate([[0, rows - 1], np.random.default_rng(mode).choice(rows, 62, replace=False)]))
