@@ -32,6 +32,7 @@ device time; the GEMM is timed in the same step and reported in TFLOP/s.
 numpy) on a bounded sample of the same workload instead.
 """
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -927,6 +928,8 @@ def main_gpu(args):
     # with the spread (FlashRT §5: re-measure before accepting a number).
     regions = []
     walls = []
+    gc.collect()
+    gc.disable()                  # no collector pause inside an event pair
     for rep in range(args.repeats):
         barrier(pg)
         torch.cuda.synchronize()
@@ -943,6 +946,7 @@ def main_gpu(args):
         for op, e0, e1 in recs:
             per_region.setdefault(op.name, []).append(e0.elapsed_time(e1))
         regions.append(per_region)
+    gc.enable()
     clk = clocks.stop()
 
     per_op = {op.name: {"op": op} for op in ops}
@@ -1043,10 +1047,11 @@ def main_gpu(args):
 
     # end to end through the C ABI with host buffers: H2D inputs, op, D2H outputs
     if not args.no_e2e:
-        e2e = measure_e2e(ops, args, stream)
+        e2e = measure_e2e(ops, args, stream, copy_streams=args.e2e_copy_streams)
         e2e_ms = max_over_ranks(pg, e2e["mem_ms"])
         line["e2e"] = {"value": round(sum_over_ranks(pg, e2e["mem_bytes"]) / (e2e_ms / 1e3) / 1e9, 1),
-                       "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
+                       "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                       "copy_streams_per_direction": e2e["copy_streams"]}
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = run_cpu_baseline()
     if rank == 0:
@@ -1127,14 +1132,17 @@ def gemm_library_reference(op, flush_l2, reps=20):
     return out
 
 
-def measure_e2e(ops, args, stream):
+def measure_e2e(ops, args, stream, copy_streams=1):
     """The memory-bound operators fed from and drained to pinned host memory,
     timed with events from the first input copy to the last output copy of a
-    step.  Within a step the operators are pipelined over three streams: the
-    inputs of operator i+1 copy in while operator i runs and the outputs of
-    operator i-1 copy out (every operator owns its device buffers; the host
-    link carries both directions at once).  Steps are separated by a
-    synchronisation."""
+    step.  Within a step the operators are pipelined: the inputs of operator
+    i+1 copy in while operator i runs and the outputs of operator i-1 copy
+    out (every operator owns its device buffers).  With `copy_streams` > 1
+    each tensor from 8 MB up is cut into that many pieces on as many streams
+    per direction; on this part that was slower in this pipeline (141-174
+    GB/s with four against 188-222 with one, the same box, alternating runs),
+    although a bare bidirectional copy gains from more streams.  Steps are
+    separated by a synchronisation."""
     import torch
     mem_ops = [op for op in ops if op.bound != "tensor"]
     host = {}
@@ -1142,37 +1150,67 @@ def measure_e2e(ops, args, stream):
         ins, outs = op.e2e_buffers()
         host[op.name] = ([t.cpu().pin_memory() for t in ins], ins, [torch.empty_like(t, device="cpu").pin_memory()
                                                                     for t in outs], outs)
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    s_in = [torch.cuda.Stream() for _ in range(copy_streams)]
+    s_out = [torch.cuda.Stream() for _ in range(copy_streams)]
     compute = torch.cuda.current_stream()
     h2d = sum(sum(t.numel() * t.element_size() for t in host[op.name][1]) for op in mem_ops)
     d2h = sum(sum(t.numel() * t.element_size() for t in host[op.name][3]) for op in mem_ops)
     mem_bytes = sum(op.algorithmic_bytes() for op in mem_ops)
+
+    big = 8 << 20                 # tensors from 8 MB up are cut into pieces; smaller ones go whole
+
+    def plan(pairs, streams):
+        """(stream, src, dst) copies: large tensors split over every stream,
+        small ones whole, dealt round-robin (thousands of tiny copies would
+        leave the host behind the link)."""
+        out, rr = [], 0
+        for src, dst in pairs:
+            if src.numel() * src.element_size() >= big:
+                for st, a, b in zip(streams, torch.chunk(src.reshape(-1), len(streams)),
+                                    torch.chunk(dst.reshape(-1), len(streams))):
+                    out.append((st, a, b))
+            else:
+                out.append((streams[rr % len(streams)], src, dst))
+                rr += 1
+        return out
+
+    plans_in = {op.name: plan(zip(host[op.name][0], host[op.name][1]), s_in) for op in mem_ops}
+    plans_out = {op.name: plan(zip(host[op.name][3], host[op.name][2]), s_out) for op in mem_ops}
     steps = max(1, min(args.steps, 3))
     times = []
     for s in range(steps + 1):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s_in)
+        e0.record(compute)
+        for st in s_in + s_out:
+            st.wait_event(e0)
         for op in mem_ops:
             hin, din, hout, dout = host[op.name]
-            with torch.cuda.stream(s_in):
-                for h, d in zip(hin, din):
-                    d.copy_(h, non_blocking=True)
-            ready = torch.cuda.Event()
-            ready.record(s_in)
-            compute.wait_event(ready)
+            for st, hp, dp in plans_in[op.name]:
+                with torch.cuda.stream(st):
+                    dp.copy_(hp, non_blocking=True)
+            for st in s_in:
+                ready = torch.cuda.Event()
+                ready.record(st)
+                compute.wait_event(ready)
             op.run()
             done = torch.cuda.Event()
             done.record(compute)
-            s_out.wait_event(done)
-            with torch.cuda.stream(s_out):
-                for h, d in zip(hout, dout):
-                    h.copy_(d, non_blocking=True)
-        e1.record(s_out)
+            for st in s_out:
+                st.wait_event(done)
+            for st, dp, hp in plans_out[op.name]:
+                with torch.cuda.stream(st):
+                    hp.copy_(dp, non_blocking=True)
+        for st in s_out:
+            fin = torch.cuda.Event()
+            fin.record(st)
+            compute.wait_event(fin)
+        e1.record(compute)
         torch.cuda.synchronize()
         if s > 0:                 # the first pass warms up
             times.append(e0.elapsed_time(e1))
-    return {"mem_ms": sum(times) / len(times), "mem_bytes": mem_bytes, "h2d": h2d, "d2h": d2h}
+    return {"mem_ms": sum(times) / len(times), "mem_bytes": mem_bytes, "h2d": h2d, "d2h": d2h,
+            "copy_streams": copy_streams}
 
 
 def main_reference(args):
@@ -1316,6 +1354,7 @@ def main():
     ap.add_argument("--no-gemm", action="store_true", help="leave the GEMM row out of the step")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--e2e-copy-streams", type=int, default=1, help="copy streams per direction in the e2e pass")
     ap.add_argument("--only", default="", help="comma-separated subset of: " + ", ".join(OP_NAMES))
     ap.add_argument("--small", action="store_true", help="profiling-size cases (still larger than L2)")
     ap.add_argument("--sweep", action="store_true",
