@@ -217,3 +217,26 @@ def test_e4m3_range_edges_four_vector_plan(gbf, kind, mode):
     c = workloads.add_rmsnorm_edge_case(2003, 8192, mode, kind, seed=80 + mode, gated=mode == 2)
     pick = np.unique(np.concatenate([[0, 1, 2002], np.random.default_rng(mode).choice(2003, 40, replace=False)]))
     check_edge(gbf, c, rows=pick, what=f"[2003,8192] {kind} mode {mode}")
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_zero_rows_with_zero_eps_are_nan_on_both_sides(gbf, mode):
+    """The degenerate case of the norm: eps = 0 on a residual row that is all
+    zeros is 0 / 0.  IEEE arithmetic makes it NaN on both sides, and the
+    saturating E4M3 conversion keeps NaN (saturation applies to finite values
+    only), so every code of those rows is a NaN code (0x7F or 0xFF) on the GPU
+    and in the oracle; every other row matches element by element."""
+    c = workloads.add_rmsnorm_edge_case(48, 512, mode, "zero_rows", seed=90 + mode)
+    c["eps"] = 0.0
+    res_out, q = run_gpu(gbf, c)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ref_res, ref_q = run_oracle(c)
+    assert_bf16_close(res_out, ref_res, "eps 0 res_out")
+    zero = np.zeros(48, bool)
+    zero[::3] = True
+    if mode != 2:
+        zero[1] = True         # x = -res: the residual sums to zero (no gate in these modes)
+    nan_codes = (0x7F, 0xFF)
+    assert np.isin(q[zero], nan_codes).all() and np.isin(ref_q[zero], nan_codes).all()
+    assert_fp8_codes(q[~zero], ref_q[~zero], f"eps 0 mode {mode} nonzero rows")
+    assert not np.isin(q[~zero], nan_codes).any()
