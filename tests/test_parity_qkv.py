@@ -115,6 +115,16 @@ def test_full_width_head_dim_48(gbf, rope):
     check(gbf, c, f"head_dim 48 rope {rope}")
 
 
+@pytest.mark.parametrize("norm,rope", [(0, 1), (1, 1), (1, 0)])
+def test_staged_ring_wraps(gbf, norm, rope):
+    """2500 tokens of 8 + 2 x 8 heads x 128 (44/42/42 sections for 3D) on the
+    staged kernel: each persistent CTA takes five or six tokens, more than its
+    ring holds, so the row buffers are refilled and the ring wraps."""
+    c = workloads.qkv_case(2500, 8, 8, 128, norm, rope, seed=70 + norm + 2 * rope, theta=1e4,
+                           grid=(10, 10, 25) if rope else None, sections=(44, 42, 42) if rope else None)
+    check(gbf, c, f"ring wraps norm {norm} rope {rope}")
+
+
 def test_3d_per_head_with_zero_section(gbf):
     c = workloads.qkv_case(11, 4, 2, 128, 0, 1, seed=3, theta=1e4, grid=(2, 3, 4), sections=(64, 0, 64))
     check(gbf, c, "3D with an empty section")
