@@ -51,7 +51,8 @@ def test_tiny_config_residual_rmsnorm_fp8(gbf):
 @pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("gated", [False, True])
 @pytest.mark.parametrize("rows,hidden", [(1, 8), (3, 64), (37, 256), (4, 512), (6, 768), (10, 1024), (5, 1032),
-                                         (7, 4096), (3, 8192), (3, 8200), (2, 16384), (2, 24576), (2, 32768)])
+                                         (7, 4096), (3, 8192), (3, 8200), (2, 16384), (2, 24576), (2, 32768),
+                                         (5, 520), (7, 1000)])
 def test_modes_and_shapes(gbf, mode, gated, rows, hidden):
     c = workloads.add_rmsnorm_case(rows, hidden, mode, seed=rows * 7 + hidden, gated=gated)
     check(gbf, c, what=f"mode {mode} gated {gated} [{rows},{hidden}]")
