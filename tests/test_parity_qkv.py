@@ -125,6 +125,30 @@ def test_staged_ring_wraps(gbf, norm, rope):
     check(gbf, c, f"ring wraps norm {norm} rope {rope}")
 
 
+@pytest.mark.parametrize("norm,rope", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_zero_tokens_and_outlier_heads(gbf, norm, rope):
+    """Padding-like tokens whose Q and K are all zero (the norm of a zero head,
+    or of a zero full-width row, is 0 * 1/sqrt(eps) = 0, so their Q and K come
+    out zero while V passes through), and heads holding one value of magnitude
+    1e4 or 3e4 that sets the head's (or the row's) scale; per-head and staged
+    kernels."""
+    c = workloads.qkv_case(24, 4, 2, 128, norm, rope, seed=80 + norm + 2 * rope, theta=1e4,
+                           grid=(2, 3, 4) if rope else None, sections=(44, 42, 42) if rope else None)
+    qkv = c["qkv"].copy()
+    d, qk = 128, (4 + 2) * 128
+    zero_tokens = [0, 5, 17]
+    qkv[zero_tokens, :qk] = 0
+    big = lambda v: np.uint16(np.array(v, np.float32).view(np.uint32) >> 16)      # noqa: E731
+    qkv[3, 1 * d + 7] = big(1e4)
+    qkv[9, 4 * d + 100] = big(-3e4)
+    qkv[12, 5 * d + 64] = big(2e4)
+    c["qkv"] = qkv
+    check(gbf, c, f"zero tokens / outliers norm {norm} rope {rope}")
+    q, kc, _ = run_gpu(gbf, c)
+    assert np.all(np.isin(q[zero_tokens], (0x0000, 0x8000)))
+    assert np.all(np.isin(kc[zero_tokens], (0x0000, 0x8000)))
+
+
 def test_3d_per_head_with_zero_section(gbf):
     c = workloads.qkv_case(11, 4, 2, 128, 0, 1, seed=3, theta=1e4, grid=(2, 3, 4), sections=(64, 0, 64))
     check(gbf, c, "3D with an empty section")
