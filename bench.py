@@ -27,6 +27,10 @@ with a barrier and a device synchronisation on both sides; the slowest rank
 counts.  `value` is the aggregate HBM throughput of the memory-bound fused
 kernels: their algorithmic bytes summed over the step divided by their summed
 device time; the GEMM is timed in the same step and reported in TFLOP/s.
+After the step, outside its aggregate, `latency_bound.qwen3_qkv_decode_paged`
+times decode-shaped QKV post-processing into a paged KV cache (32 sequences'
+new tokens, K/V rows by slot mapping into 16-row blocks of a 16,384-row
+cache): 100 calls as one CUDA graph, microseconds per call.
 
 `--impl reference` times the CPU oracle (the unfused operator chains, float64
 numpy) on a bounded sample of the same workload instead.
@@ -1045,6 +1049,11 @@ def main_gpu(args):
                                                                 args.gemm_sustained_s)
         line["roofline_gemm"]["library_same_box"] = gemm_library_reference(per_op["linear_bias_gelu"]["op"], flush_l2)
 
+    # decode-shaped QKV into a paged KV cache: launch-bound, timed on its own
+    # (outside the step, so the step's aggregate keeps its composition)
+    if "qwen3_qkv" in per_op:
+        line["latency_bound"]["qwen3_qkv_decode_paged"] = measure_decode_paged(gbf, flush_l2)
+
     # end to end through the C ABI with host buffers: H2D inputs, op, D2H outputs
     if not args.no_e2e:
         e2e = measure_e2e(ops, args, stream, copy_streams=args.e2e_copy_streams)
@@ -1058,6 +1067,58 @@ def main_gpu(args):
         print(json.dumps(line))
     if pg is not None:
         pg.destroy_process_group()
+
+
+def measure_decode_paged(gbf, flush_l2, calls=100, reps=20):
+    """Decode-shaped QKV post-processing into a paged KV cache
+    (workloads.qkv_decode_paged_case: 32 sequences' new tokens, Qwen3's 32 +
+    2 x 8 heads x 128, per-head RMSNorm and 1D RoPE, K/V rows by slot mapping
+    into a 16,384-row cache of 16-row blocks): `calls` calls captured through
+    the C ABI into one CUDA graph, replayed after an L2 flush; per-call
+    microseconds, median over `reps` replays."""
+    import torch
+    import workloads
+    from workloads import as_torch as from_bits
+    c = workloads.qkv_decode_paged_case()
+    t, hq, hkv, d = c["tokens"], c["n_q"], c["n_kv"], c["d"]
+    qkv, qw, kw = from_bits(c["qkv"]), from_bits(c["q_w"]), from_bits(c["k_w"])
+    pos = torch.from_numpy(c["pos"]).cuda()
+    slots = torch.from_numpy(c["slots"]).cuda()
+    q = torch.empty(t, hq, d, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(c["cache_rows"], hkv, d, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+
+    def call():
+        gbf.qkv_split_norm_rope(qkv, hq, hkv, d, gbf.QKNORM_PER_HEAD, qw, kw, c["eps"], gbf.ROPE_1D, pos,
+                                c["theta"], q, kc, vc, slots=slots, cache_rows=c["cache_rows"])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(calls):
+            call()
+    torch.cuda.synchronize()
+    ts = []
+    for it in range(reps + 3):
+        flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if it >= 3:
+            ts.append(e0.elapsed_time(e1))
+    status, msg = gbf.device_status()
+    if status != gbf.OK:
+        raise RuntimeError(f"device status after the decode graph: {msg}")
+    ms = statistics.median(ts)
+    return {"us_per_launch": round(ms * 1e3 / calls, 3), "launches": calls, "tokens": t,
+            "cache_rows": c["cache_rows"], "block_rows": 16, "bytes_per_launch": bytes_qkv(t, hq, hkv, d),
+            "note": "timed on its own after the step (not part of the step's aggregate)"}
 
 
 def gemm_sustained(op, cuda_index, peaks, seconds):

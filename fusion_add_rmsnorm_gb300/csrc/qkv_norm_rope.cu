@@ -292,6 +292,9 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   const __nv_bfloat16* row = static_cast<const __nv_bfloat16*>(a.qkv) + t * static_cast<int64_t>(heads) * D;
   uint4 lo[kRotBatch], hi[kRotBatch];
   if (live) rot1d_load<LPH, G>(row, grp, heads, lane, lo, hi);
+  // the token's cache row is requested with its data, not after the table
+  bool slot_ok = false;
+  const int64_t crow = live ? cache_slot(a, t, slot_ok) : 0;
 
   __shared__ float4 cs4[TOK * 4 * LPH];
   {
@@ -301,8 +304,6 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   }
   __syncthreads();
   if (!live) return;
-  bool slot_ok;
-  const int64_t crow = cache_slot(a, t, slot_ok);
   if (!slot_ok && threadIdx.x % TPT == 0) raise_error(a.err, DEV_ERR_SLOT_RANGE);
   float2 c2[4], s2[4];
   rot1d_cs_read<LPH>(cs4 + tok * 4 * LPH, lane, c2, s2);

@@ -172,6 +172,22 @@ def test_slots_scatter_into_a_larger_cache(gbf, norm, rope):
     assert s == gbf.OK
 
 
+def test_decode_paged_cache(gbf):
+    """The decode shape the bench times for the paged cache: 32 sequences'
+    new tokens at scattered positions, each K/V row written to its block's
+    slot of a 16,384-row cache; every other cache row stays untouched."""
+    c = workloads.qkv_decode_paged_case()
+    q, kc, vc = run_gpu(gbf, c, slots=c["slots"], cache_rows=c["cache_rows"])
+    rq, rk, rv = run_oracle(c, slots=c["slots"], cache_rows=c["cache_rows"])
+    assert_bf16_close(q, rq, "Q")
+    assert_bf16_close(kc[c["slots"]], rk[c["slots"]], "K cache rows")
+    assert np.array_equal(vc, rv)
+    untouched = np.setdiff1d(np.arange(c["cache_rows"]), c["slots"])
+    assert not kc[untouched].any() and not vc[untouched].any()
+    s, _ = gbf.device_status()
+    assert s == gbf.OK
+
+
 @pytest.mark.parametrize("norm,rope", [(0, 0), (1, 1)])
 def test_out_of_range_slot_is_skipped_and_reported(gbf, norm, rope):
     """A slot outside the cache writes nothing for that token and raises the

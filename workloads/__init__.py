@@ -160,6 +160,25 @@ def config_qwen3_qkv(seed=0, tokens=4096):
     return qkv_case(tokens, 32, 8, 128, 0, 0, seed, theta=1e6)
 
 
+def qkv_decode_paged_case(tokens=32, n_q_heads=32, n_kv_heads=8, head_dim=128, cache_rows=16384, block=16,
+                          max_pos=4096, seed=0):
+    """Decode-shaped QKV post-processing into a paged KV cache: one new token
+    per sequence, `tokens` sequences with Qwen3's heads; packed QKV and
+    weights as qkv_case (per-head RMSNorm, 1D RoPE theta 1e6); each
+    sequence's position drawn uniformly in [0, max_pos); the cache is
+    cache_rows // block blocks of `block` rows, each sequence owning a
+    distinct block drawn without replacement, and its token's slot is that
+    block's row (position mod block), the slot mapping of a paged cache."""
+    c = qkv_case(tokens, n_q_heads, n_kv_heads, head_dim, 0, 0, seed, theta=1e6)
+    rng = np.random.Generator(np.random.PCG64(seed + 2000))
+    pos = rng.integers(0, max_pos, size=tokens).astype(np.int32)
+    blocks = rng.choice(cache_rows // block, size=tokens, replace=False).astype(np.int64)
+    c["pos"] = pos
+    c["slots"] = (blocks * block + pos % block).astype(np.int32)
+    c["cache_rows"] = cache_rows
+    return c
+
+
 def layernorm_qkv_case(tokens, n_q_heads, n_kv_heads, head_dim, seed=0, theta=1e4, biases=True):
     """Packed QKV bf16 [tokens, (Hq + 2 Hkv) * D] ~ N(0,1); then q_w, k_w =
     1 + N(0, 0.1) and (when `biases`) q_b, k_b ~ N(0, 0.1), all [D]; eps 1e-5;
