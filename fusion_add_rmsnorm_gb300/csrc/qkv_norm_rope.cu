@@ -32,10 +32,11 @@
 //    l + D/16, which contain both members of its 8 rotation pairs (j, j + D/2),
 //    so the rotation is done in registers and the head's statistics are a
 //    shuffle reduction over the head's lanes.  Each thread visits every G-th
-//    head of its token (G = 8, 16 or 32 head groups, a token's G * D/16
-//    threads at most 128; V heads are copied), issuing a batch of loads before
-//    any arithmetic, and the token's (cos, sin) are computed once per token
-//    into a shared table.
+//    head of its token (G head groups, a power of two: a token's G * D/16
+//    threads at most 128 in streaming launches, up to 512 with one head per
+//    group in launch-bound ones; V heads are copied), issuing a batch of loads
+//    before any arithmetic, and the token's (cos, sin) are computed once per
+//    token into a shared table.
 //  * qkv_staged_kernel (everything else: full-width norm and/or 3D sections,
 //    where a rotation pair need not sit in one 16-byte vector): a persistent
 //    CTA streams its tokens' packed rows through a ring of shared-memory
@@ -78,12 +79,6 @@ struct __align__(16) SlotEntry {
   float om_hi, om_lo;
   int lo, hi_axis;        // hi_axis = hi | axis << 16
 };
-
-GBF_DEVICE int64_t cache_slot(const QkvArgs& a, int64_t t, bool& ok) {
-  const int64_t slot = a.slots ? static_cast<int64_t>(a.slots[t]) : t;
-  ok = slot >= 0 && slot < a.cache_rows;
-  return slot;
-}
 
 // --------------------------------------------------------- per-head, 1D
 
@@ -265,11 +260,12 @@ GBF_DEVICE void rot1d_cs_read(const float4* cs_tok, int lane, float2 (&c2)[4], f
   }
 }
 
-// Threads per CTA of the per-head kernel: 128 where a token's G * LPH threads
-// fit, else 256.  The smaller CTA ends sooner (its share of the bandwidth
-// moves fewer tokens), so the tail of a launch, where the last CTAs run
-// alone, is shorter; the registers per thread are the same either way.
-constexpr int rot1d_block(int g, int lph) { return g * lph <= 128 ? 128 : kRotBlock; }
+// Threads per CTA of the per-head kernel: the smallest of 128, 256 and 512
+// that holds a token's G * LPH threads.  For streaming launches the smaller
+// CTA ends sooner (its share of the bandwidth moves fewer tokens), so the
+// tail of a launch, where the last CTAs run alone, is shorter; the registers
+// per thread are the same either way.
+constexpr int rot1d_block(int g, int lph) { return g * lph <= 128 ? 128 : g * lph <= 256 ? kRotBlock : 512; }
 
 // One CTA per TOK tokens; a thread with more than one batch of heads takes
 // them in turn.  The first batch is requested before the (cos, sin) table.
@@ -292,9 +288,9 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   const __nv_bfloat16* row = static_cast<const __nv_bfloat16*>(a.qkv) + t * static_cast<int64_t>(heads) * D;
   uint4 lo[kRotBatch], hi[kRotBatch];
   if (live) rot1d_load<LPH, G>(row, grp, heads, lane, lo, hi);
-  // the token's cache row is requested with its data, not after the table
-  bool slot_ok = false;
-  const int64_t crow = live ? cache_slot(a, t, slot_ok) : 0;
+  // the token's cache row (slot mapping) is requested with its data, not
+  // after the table
+  const int32_t slot_in = live && a.slots ? a.slots[t] : 0;
 
   __shared__ float4 cs4[TOK * 4 * LPH];
   {
@@ -304,6 +300,8 @@ qkv_rot1d_kernel(const __grid_constant__ QkvArgs a) {
   }
   __syncthreads();
   if (!live) return;
+  const int64_t crow = a.slots ? static_cast<int64_t>(slot_in) : t;
+  const bool slot_ok = crow >= 0 && crow < a.cache_rows;
   if (!slot_ok && threadIdx.x % TPT == 0) raise_error(a.err, DEV_ERR_SLOT_RANGE);
   float2 c2[4], s2[4];
   rot1d_cs_read<LPH>(cs4 + tok * 4 * LPH, lane, c2, s2);
@@ -723,22 +721,37 @@ cudaError_t launch_rot1d_g(const QkvArgs& a, cudaStream_t stream) {
   return launch_pdl(qkv_rot1d_kernel<LPH, false, G, BLOCK>, dim3(grid), dim3(BLOCK), 0, stream, a);
 }
 
-// G = the smallest of 8, 16, 32 head groups that leaves a thread at most
-// kRotBatch heads, within the 128 threads a token may use: a thread with more
-// heads takes them in batches.  One token per 128-thread CTA measured faster
-// than one per 256-thread CTA with a single batch (Qwen3, 48 heads: 17.1 vs
-// 19.6 us; Chameleon, 96 heads: 32.8 vs 34.8 us): the CTAs that run alone at
-// the end of the launch are shorter.
+// G, the head groups of a token (a power of two from 8 up):
+//  * streaming launches (more tokens than SMs): the smallest G that leaves a
+//    thread at most kRotBatch heads, within the 128 threads a token may use
+//    (a thread with more heads takes them in batches).  One token per
+//    128-thread CTA measured faster than one per 256-thread CTA with a single
+//    batch (Qwen3, 48 heads: 17.1 vs 19.6 us; Chameleon, 96 heads: 32.8 vs
+//    34.8 us): the CTAs that run alone at the end of the launch are shorter.
+//  * launch-bound ones (at most one token per SM, e.g. decode): a group per
+//    head, up to 512 threads per token, so a thread's critical path is one
+//    head (Qwen3 decode, 32 tokens into a paged cache: 2.16-2.28 us per call
+//    against 2.52-2.59 with 128-thread CTAs).
 template <int LPH>
 cudaError_t launch_rot1d(const QkvArgs& a, cudaStream_t stream) {
   const int heads = a.n_q + 2 * a.n_kv;
-  constexpr int gmax = 128 / LPH;            // 32, 16, 8 for head_dim 64, 128, 256
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int g = 8;
-  while (g < gmax && g * kRotBatch < heads) g *= 2;
-  if constexpr (gmax >= 32)
-    if (g == 32) return launch_rot1d_g<LPH, 32>(a, stream);
-  if constexpr (gmax >= 16)
-    if (g == 16) return launch_rot1d_g<LPH, 16>(a, stream);
+  if (a.tokens <= sms) {
+    constexpr int gwide = 512 / LPH;         // 128, 64, 32 for head_dim 64, 128, 256
+    while (g < gwide && g < heads) g *= 2;
+  } else {
+    constexpr int gmax = 128 / LPH;          // 32, 16, 8
+    while (g < gmax && g * kRotBatch < heads) g *= 2;
+  }
+  if constexpr (512 / LPH >= 128)
+    if (g == 128) return launch_rot1d_g<LPH, 128>(a, stream);
+  if constexpr (512 / LPH >= 64)
+    if (g == 64) return launch_rot1d_g<LPH, 64>(a, stream);
+  if (g == 32) return launch_rot1d_g<LPH, 32>(a, stream);
+  if (g == 16) return launch_rot1d_g<LPH, 16>(a, stream);
   return launch_rot1d_g<LPH, 8>(a, stream);
 }
 
