@@ -30,7 +30,8 @@ device time; the GEMM is timed in the same step and reported in TFLOP/s.
 After the step, outside its aggregate, `latency_bound.qwen3_qkv_decode_paged`
 times decode-shaped QKV post-processing into a paged KV cache (32 sequences'
 new tokens, K/V rows by slot mapping into 16-row blocks of a 16,384-row
-cache): 100 calls as one CUDA graph, microseconds per call.
+cache), and `latency_bound.swiglu_decode` SwiGLU on [32, 2 x 11008]: 100
+calls as one CUDA graph each, microseconds per call.
 
 `--impl reference` times the CPU oracle (the unfused operator chains, float64
 numpy) on a bounded sample of the same workload instead.
@@ -1053,6 +1054,8 @@ def main_gpu(args):
     # (outside the step, so the step's aggregate keeps its composition)
     if "qwen3_qkv" in per_op:
         line["latency_bound"]["qwen3_qkv_decode_paged"] = measure_decode_paged(gbf, flush_l2)
+    if "swiglu_ffn" in per_op:
+        line["latency_bound"]["swiglu_decode"] = measure_swiglu_decode(gbf, flush_l2)
 
     # end to end through the C ABI with host buffers: H2D inputs, op, D2H outputs
     if not args.no_e2e:
@@ -1069,28 +1072,11 @@ def main_gpu(args):
         pg.destroy_process_group()
 
 
-def measure_decode_paged(gbf, flush_l2, calls=100, reps=20):
-    """Decode-shaped QKV post-processing into a paged KV cache
-    (workloads.qkv_decode_paged_case: 32 sequences' new tokens, Qwen3's 32 +
-    2 x 8 heads x 128, per-head RMSNorm and 1D RoPE, K/V rows by slot mapping
-    into a 16,384-row cache of 16-row blocks): `calls` calls captured through
-    the C ABI into one CUDA graph, replayed after an L2 flush; per-call
-    microseconds, median over `reps` replays."""
+def graph_latency_us(gbf, call, flush_l2, calls=100, reps=20):
+    """`calls` back-to-back calls of `call` captured through the C ABI into one
+    CUDA graph, replayed `reps` times after an L2 flush; median microseconds
+    per call."""
     import torch
-    import workloads
-    from workloads import as_torch as from_bits
-    c = workloads.qkv_decode_paged_case()
-    t, hq, hkv, d = c["tokens"], c["n_q"], c["n_kv"], c["d"]
-    qkv, qw, kw = from_bits(c["qkv"]), from_bits(c["q_w"]), from_bits(c["k_w"])
-    pos = torch.from_numpy(c["pos"]).cuda()
-    slots = torch.from_numpy(c["slots"]).cuda()
-    q = torch.empty(t, hq, d, dtype=torch.bfloat16, device="cuda")
-    kc = torch.zeros(c["cache_rows"], hkv, d, dtype=torch.bfloat16, device="cuda")
-    vc = torch.zeros_like(kc)
-
-    def call():
-        gbf.qkv_split_norm_rope(qkv, hq, hkv, d, gbf.QKNORM_PER_HEAD, qw, kw, c["eps"], gbf.ROPE_1D, pos,
-                                c["theta"], q, kc, vc, slots=slots, cache_rows=c["cache_rows"])
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
@@ -1114,10 +1100,50 @@ def measure_decode_paged(gbf, flush_l2, calls=100, reps=20):
             ts.append(e0.elapsed_time(e1))
     status, msg = gbf.device_status()
     if status != gbf.OK:
-        raise RuntimeError(f"device status after the decode graph: {msg}")
-    ms = statistics.median(ts)
-    return {"us_per_launch": round(ms * 1e3 / calls, 3), "launches": calls, "tokens": t,
+        raise RuntimeError(f"device status after a latency graph: {msg}")
+    return statistics.median(ts) * 1e3 / calls
+
+
+def measure_decode_paged(gbf, flush_l2, calls=100):
+    """Decode-shaped QKV post-processing into a paged KV cache
+    (workloads.qkv_decode_paged_case: 32 sequences' new tokens, Qwen3's 32 +
+    2 x 8 heads x 128, per-head RMSNorm and 1D RoPE, K/V rows by slot mapping
+    into a 16,384-row cache of 16-row blocks), per-call microseconds."""
+    import torch
+    import workloads
+    from workloads import as_torch as from_bits
+    c = workloads.qkv_decode_paged_case()
+    t, hq, hkv, d = c["tokens"], c["n_q"], c["n_kv"], c["d"]
+    qkv, qw, kw = from_bits(c["qkv"]), from_bits(c["q_w"]), from_bits(c["k_w"])
+    pos = torch.from_numpy(c["pos"]).cuda()
+    slots = torch.from_numpy(c["slots"]).cuda()
+    q = torch.empty(t, hq, d, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(c["cache_rows"], hkv, d, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+
+    def call():
+        gbf.qkv_split_norm_rope(qkv, hq, hkv, d, gbf.QKNORM_PER_HEAD, qw, kw, c["eps"], gbf.ROPE_1D, pos,
+                                c["theta"], q, kc, vc, slots=slots, cache_rows=c["cache_rows"])
+    us = graph_latency_us(gbf, call, flush_l2, calls)
+    return {"us_per_launch": round(us, 3), "launches": calls, "tokens": t,
             "cache_rows": c["cache_rows"], "block_rows": 16, "bytes_per_launch": bytes_qkv(t, hq, hkv, d),
+            "note": "timed on its own after the step (not part of the step's aggregate)"}
+
+
+def measure_swiglu_decode(gbf, flush_l2, rows=32, d=11008, calls=100):
+    """SwiGLU silu(gate) * up on a decode batch: [rows, 2 x 11008] bf16
+    (workloads.config_swiglu_ffn's row width and draws), per-call
+    microseconds."""
+    import workloads
+    from workloads import as_torch as from_bits
+    c = workloads.config_swiglu_ffn(rows=rows)
+    x = from_bits(c["x"])
+    y = x.new_empty(rows, d)
+
+    def call():
+        gbf.gated_act(x, y, gbf.ACT_SILU)
+    us = graph_latency_us(gbf, call, flush_l2, calls)
+    return {"us_per_launch": round(us, 3), "launches": calls, "rows": rows, "bytes_per_launch": rows * d * 6,
             "note": "timed on its own after the step (not part of the step's aggregate)"}
 
 

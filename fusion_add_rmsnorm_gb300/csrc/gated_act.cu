@@ -11,7 +11,10 @@
 // Design: each row is cut into equal tiles of at most kGaUnroll * kGaBlock
 // 16-byte vectors; persistent CTAs walk the (row, tile) pairs (grid-stride),
 // each thread issuing its (up to kGaUnroll) gate and up loads before any
-// arithmetic; float32 math, one bf16 rounding, 16-byte stores.  SiLU uses
+// arithmetic; float32 math, one bf16 rounding, 16-byte stores.  A launch
+// with fewer (row, tile) pairs than SMs (a decode batch) cuts its rows into
+// more, smaller tiles (down to 64 vectors, at most one tile per SM), so the
+// work spreads over the SMs and a thread's critical path is about one vector.  SiLU uses
 // the fast exponential and division intrinsics and the tanh GELU the
 // hardware tanh approximation (both well inside a bf16 rounding); the erf
 // GELU calls erff.  Launched with programmatic dependent launch.
@@ -38,7 +41,7 @@ __global__ void __launch_bounds__(kGaBlock) gated_act_kernel(const GatedActArgs 
   pdl_wait();
   pdl_launch_dependents();
   const int64_t nv = a.d >> 3;                 // 16-byte vectors per half row
-  const int64_t tiles_per_row = (nv + kGaUnroll * kGaBlock - 1) / (kGaUnroll * kGaBlock);
+  const int64_t tiles_per_row = a.tiles_per_row;
   const int64_t per_tile = (nv + tiles_per_row - 1) / tiles_per_row;
   const int64_t tiles = a.rows * tiles_per_row;
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
@@ -94,9 +97,17 @@ cudaError_t launch_act(const GatedActArgs& a, cudaStream_t stream) {
   }
   const int64_t resident = static_cast<int64_t>(sms) * per_sm;
   const int64_t nv = a.d >> 3;
-  const int64_t tiles = a.rows * ((nv + kGaUnroll * kGaBlock - 1) / (kGaUnroll * kGaBlock));
+  GatedActArgs b = a;
+  b.tiles_per_row = (nv + kGaUnroll * kGaBlock - 1) / (kGaUnroll * kGaBlock);
+  const int64_t fit = sms / a.rows;                       // tiles per row with at most one per SM
+  if (fit > b.tiles_per_row) {
+    const int64_t most = (nv + 63) / 64;                  // tiles of at least 64 vectors
+    b.tiles_per_row = fit < most ? fit : most;
+    if (b.tiles_per_row < 1) b.tiles_per_row = 1;
+  }
+  const int64_t tiles = a.rows * b.tiles_per_row;
   const unsigned grid = static_cast<unsigned>(tiles < resident ? tiles : resident);
-  return launch_pdl(gated_act_kernel<ACT>, dim3(grid), dim3(kGaBlock), 0, stream, a);
+  return launch_pdl(gated_act_kernel<ACT>, dim3(grid), dim3(kGaBlock), 0, stream, b);
 }
 
 }  // namespace

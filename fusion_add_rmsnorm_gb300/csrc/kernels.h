@@ -83,6 +83,7 @@ struct GatedActArgs {
   void* y;                // bf16 [rows, d]
   int64_t rows, d;
   int act;
+  int64_t tiles_per_row;  // set by the launcher
 };
 
 cudaError_t launch_gated_act(const GatedActArgs& a, cudaStream_t stream);
