@@ -28,7 +28,8 @@ def run_gpu(gbf, c, act):
 
 
 @pytest.mark.parametrize("name", list(ACTS))
-@pytest.mark.parametrize("rows,d", [(1, 8), (3, 64), (37, 1032), (5, 4096), (300, 11008), (2, 2056)])
+@pytest.mark.parametrize("rows,d", [(1, 8), (3, 64), (37, 1032), (5, 4096), (300, 11008), (2, 2056),
+                                    (8, 11008), (32, 11008), (151, 1032)])
 def test_shapes(gbf, name, rows, d):
     c = workloads.gated_act_case(rows, d, seed=rows + d)
     y = run_gpu(gbf, c, ACTS[name])
