@@ -386,8 +386,10 @@ AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden, int mode) {
     // Vectors per thread: 2 for streaming launches (half the per-row
     // reduction and loop work per element), and for rows of 2048 values or
     // more in smaller ones (half the warps a row reduces over); 1 for
-    // AdaRMSNorm rows in launches of more rows than SMs, whose two-vector
-    // factors would sit in shared memory; more when a row would need more
+    // AdaRMSNorm rows in launches of one to four rows per SM, where the
+    // shared-memory copy of two-vector factors costs more than it saves
+    // ([256, 4096]: 4.35 us with one vector against 4.6-4.9 with two;
+    // [2048, 4096]: 15.3 against 12.3-12.6); more when a row would need more
     // than the block's threads.  Factors: float32 in registers where they fit
     // (one vector, or two without AdaRMSNorm); in a launch of at most one row
     // per SM, packed in registers up to four vectors (no shared-memory copy
@@ -396,7 +398,8 @@ AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden, int mode) {
     // graphs: [32, 8192] gated AdaRMSNorm 2.32 us against 3.22 with shared
     // factors, [128, 4096] weighted 2.24 against 2.75-2.81 with one vector.
     const bool latency = rows <= sm_count();
-    const int target = large || (nvec >= 256 && (mode != kNormAda || latency)) ? 2 : 1;
+    const int target =
+        large || (nvec >= 256 && (mode != kNormAda || latency || rows > 4LL * sm_count())) ? 2 : 1;
     while (nv < 8 && ((nv < target && nvec >= 16 * nv) || nvec > static_cast<int64_t>(nv) * max_block(nv)))
       nv *= 2;
     p.fac = nv == 1 || (nv == 2 && mode != kNormAda) ? kFacReg : (latency && nv <= 4 ? kFacPack : kFacSmem);
