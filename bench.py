@@ -30,8 +30,10 @@ device time; the GEMM is timed in the same step and reported in TFLOP/s.
 After the step, outside its aggregate, `latency_bound.qwen3_qkv_decode_paged`
 times decode-shaped QKV post-processing into a paged KV cache (32 sequences'
 new tokens, K/V rows by slot mapping into 16-row blocks of a 16,384-row
-cache), and `latency_bound.swiglu_decode` SwiGLU on [32, 2 x 11008]: 100
-calls as one CUDA graph each, microseconds per call.
+cache), `latency_bound.swiglu_decode` SwiGLU on [32, 2 x 11008] and
+`latency_bound.linear_decode` the Linear + bias + GELU on 32 rows (W-read
+bound; cuBLASLt's fused epilogue beside it): CUDA graphs of back-to-back
+calls, microseconds per call.
 
 `--impl reference` times the CPU oracle (the unfused operator chains, float64
 numpy) on a bounded sample of the same workload instead.
@@ -1056,6 +1058,8 @@ def main_gpu(args):
         line["latency_bound"]["qwen3_qkv_decode_paged"] = measure_decode_paged(gbf, flush_l2)
     if "swiglu_ffn" in per_op:
         line["latency_bound"]["swiglu_decode"] = measure_swiglu_decode(gbf, flush_l2)
+    if "linear_bias_gelu" in per_op:
+        line["latency_bound"]["linear_decode"] = measure_linear_decode(gbf, flush_l2)
 
     # end to end through the C ABI with host buffers: H2D inputs, op, D2H outputs
     if not args.no_e2e:
@@ -1144,6 +1148,31 @@ def measure_swiglu_decode(gbf, flush_l2, rows=32, d=11008, calls=100):
         gbf.gated_act(x, y, gbf.ACT_SILU)
     us = graph_latency_us(gbf, call, flush_l2, calls)
     return {"us_per_launch": round(us, 3), "launches": calls, "rows": rows, "bytes_per_launch": rows * d * 6,
+            "note": "timed on its own after the step (not part of the step's aggregate)"}
+
+
+def measure_linear_decode(gbf, flush_l2, m=32, calls=50):
+    """The config's Linear + bias + GELU (N 16384, K 4096) on a decode batch of
+    m rows, where reading W bounds the call: `calls` calls in one CUDA graph,
+    per-call microseconds, with cuBLASLt's fused bias + GELU on the same
+    operands timed the same way (a comparison only)."""
+    import torch
+    import workloads
+    from workloads import as_torch as from_bits
+    c = workloads.linear_gelu_case(m, 16384, 4096, seed=0)
+    x, w, b = from_bits(c["x"]), from_bits(c["w"]), from_bits(c["bias"])
+    y = torch.empty(m, 16384, dtype=torch.bfloat16, device="cuda")
+
+    def ours():
+        gbf.linear_bias_gelu(x, w, b, y, act=gbf.ACT_GELU_TANH)
+
+    def lt():
+        torch._addmm_activation(b, x, w.t(), use_gelu=True)
+    us = graph_latency_us(gbf, ours, flush_l2, calls)
+    us_lt = graph_latency_us(gbf, lt, flush_l2, calls)
+    w_bytes = 16384 * 4096 * 2
+    return {"us_per_launch": round(us, 2), "launches": calls, "rows": m, "w_bytes": w_bytes,
+            "gbs_of_w": round(w_bytes / us / 1e3, 1), "cublaslt_bias_gelu_us": round(us_lt, 2),
             "note": "timed on its own after the step (not part of the step's aggregate)"}
 
 

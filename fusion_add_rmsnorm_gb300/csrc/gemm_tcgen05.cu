@@ -10,7 +10,8 @@
 // (three HBM passes become one); npu_linear of the MindIE-SD RFC, §3.5.
 //
 // Design (persistent, one CTA per SM; CTA pairs when M spans two tiles):
-//   tiles      each CTA owns a BM x BN = 128 x 256 output tile; BK = one
+//   tiles      each CTA owns a BM x BN = 128 x 256 output tile (128 x 128 for a
+//              single M tile with fewer 256-wide N tiles than SMs); BK = one
 //              128-byte swizzle row of K (64 bf16 or 128 E4M3) per k-block.
 //   pairs      a cluster of two CTAs on vertically adjacent M tiles runs as
 //              one tcgen05 CTA pair (cta_group::2): the even CTA issues
@@ -63,11 +64,13 @@ namespace gbf {
 namespace {
 
 constexpr int BM = 128;                          // output rows per CTA (TMEM lanes)
-constexpr int BN = 256;
+constexpr int BN = 256;                          // N tile (CTA pairs and most unpaired launches)
+constexpr int BN_NARROW = 128;                   // N tile of unpaired launches with few tiles
 constexpr int BK_BYTES = 128;                    // one 128-byte swizzle row of K per k-block
 constexpr int UMMA_K_BYTES = 32;                 // K of one MMA: 16 bf16 or 32 E4M3 values
 constexpr int A_STAGE_BYTES = BM * BK_BYTES;     // 16 KB
-constexpr int TMEM_COLS = 2 * BN;                // two accumulators (all 512 columns)
+// TMEM columns: two float32 accumulators of the N tile (all 512 at BN)
+constexpr int tmem_cols(int tn) { return 2 * tn; }
 constexpr int kThreads = 384;
 constexpr int kEpilogueWarp0 = 4;                // warps 4..11: two per TMEM lane quarter
 constexpr int kEpilogueWarps = 8;
@@ -79,11 +82,12 @@ constexpr int kOutBoxBytes = 32 * kOutCols * 2;              // 4 KB
 constexpr int kOutBytes = kEpilogueWarps * kOutBoxBytes;      // 32 KB
 
 // Shared-memory ring of one CTA: unpaired, the whole W tile per stage; paired,
-// half of it (the other half sits in the other CTA).
-template <bool PAIR>
+// half of it (the other half sits in the other CTA).  32 KB stages take a
+// six-deep ring, 48 KB ones (unpaired, 256-wide) three.
+template <bool PAIR, int TN>
 struct Ring {
-  static constexpr int kStages = PAIR ? 6 : 3;
-  static constexpr int kBRows = PAIR ? BN / 2 : BN;
+  static constexpr int kBRows = PAIR ? TN / 2 : TN;
+  static constexpr int kStages = A_STAGE_BYTES + kBRows * BK_BYTES <= 32768 ? 6 : 3;
   static constexpr int kBStageBytes = kBRows * BK_BYTES;
   static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes;
 };
@@ -100,10 +104,10 @@ struct __align__(8) SharedCtl {
   int abort;
 };
 
-template <bool PAIR>
+template <bool PAIR, int TN>
 constexpr size_t smem_bytes() {
-  return 1024 /* alignment slack */ + Ring<PAIR>::kStages * Ring<PAIR>::kStageBytes + kOutBytes +
-         sizeof(SharedCtl<Ring<PAIR>::kStages>);
+  return 1024 /* alignment slack */ + Ring<PAIR, TN>::kStages * Ring<PAIR, TN>::kStageBytes + kOutBytes +
+         sizeof(SharedCtl<Ring<PAIR, TN>::kStages>);
 }
 
 // ------------------------------------------------------------ PTX wrappers
@@ -181,26 +185,26 @@ GBF_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_syn
 // Every tcgen05 instruction of one kernel names the same CTA group: 1 when
 // unpaired, 2 in a pair.
 template <bool PAIR>
-GBF_DEVICE void tmem_alloc(uint32_t* dst) {
+GBF_DEVICE void tmem_alloc(uint32_t* dst, uint32_t cols) {
   if (PAIR) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
-                 "r"(TMEM_COLS)
+                 "r"(cols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   } else {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
-                 "r"(TMEM_COLS)
+                 "r"(cols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
 }
 
 template <bool PAIR>
-GBF_DEVICE void tmem_dealloc(uint32_t base) {
+GBF_DEVICE void tmem_dealloc(uint32_t base, uint32_t cols) {
   if (PAIR)
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols) : "memory");
   else
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols) : "memory");
 }
 
 // Arrive on `bar` once the tensor-core work issued so far has completed:
@@ -292,8 +296,8 @@ GBF_DEVICE uint64_t smem_desc_sw128(uint32_t addr) {
 // Instruction descriptors: float32 D (bits 4-5 = 1), A and B type codes at
 // bits 7-9 and 10-12 (kind::f16: bf16 = 1; kind::f8f6f4: E4M3 = 0), both
 // K-major, N >> 3 at bit 17, M >> 4 at bit 24 (M = 256 for a CTA pair).
-__host__ __device__ constexpr uint32_t idesc(bool fp8, int m) {
-  return (1u << 4) | ((fp8 ? 0u : 1u) << 7) | ((fp8 ? 0u : 1u) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+__host__ __device__ constexpr uint32_t idesc(bool fp8, int m, int n) {
+  return (1u << 4) | ((fp8 ? 0u : 1u) << 7) | ((fp8 ? 0u : 1u) << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
@@ -312,25 +316,25 @@ struct GemmParams {
 // above).  With CTA pairs a work item is two vertically adjacent M tiles
 // sharing one W column block: m_units = ceil(m_tiles / cl), and CTA rank
 // `rank` of the pair takes M tile unit * cl + rank.
-GBF_DEVICE void tile_origin(const GemmParams& p, int m_units, int cl, int rank, int tile, int& m0, int& n0) {
+GBF_DEVICE void tile_origin(const GemmParams& p, int m_units, int cl, int rank, int tile, int tn, int& m0, int& n0) {
   const int per_group = p.group_n * m_units;
   const int g = tile / per_group;
   const int idx = tile - g * per_group;
   const int n_base = g * p.group_n;
   const int gs = p.n_tiles - n_base < p.group_n ? p.n_tiles - n_base : p.group_n;
   m0 = ((idx / gs) * cl + rank) * BM;
-  n0 = (n_base + idx % gs) * BN;
+  n0 = (n_base + idx % gs) * tn;
 }
 
-template <bool FP8, bool PAIR>
+template <bool FP8, bool PAIR, int TN>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                         const __grid_constant__ CUtensorMap map_y, const GemmParams p) {
-  using R = Ring<PAIR>;
+  using R = Ring<PAIR, TN>;
   constexpr int S = R::kStages;
   constexpr int CL = PAIR ? 2 : 1;
   constexpr int BK = FP8 ? BK_BYTES : BK_BYTES / 2;         // K elements per k-block
-  constexpr uint32_t kIdesc = idesc(FP8, CL * BM);
+  constexpr uint32_t kIdesc = idesc(FP8, CL * BM, TN);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the same offsets in both CTAs of a pair: the MMAs address the odd CTA's
   // operands by the even CTA's shared addresses
@@ -365,7 +369,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_y)) : "memory");
   }
-  if (warp == 2) tmem_alloc<PAIR>(&ctl->tmem_base);
+  if (warp == 2) tmem_alloc<PAIR>(&ctl->tmem_base, tmem_cols(TN));
   tc_fence_before();
   __syncthreads();
   if (PAIR) cluster_sync();                // both CTAs' barriers and TMEM exist before either is used
@@ -393,7 +397,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       bool ok = true;
       for (int tile = first; tile < num_tiles && ok; tile += stride) {
         int m0, n0;
-        tile_origin(p, m_units, CL, rank, tile, m0, n0);
+        tile_origin(p, m_units, CL, rank, tile, TN, m0, n0);
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait<PAIR, false>(&ctl->empty[stage], phase ^ 1u, &ctl->abort, p.err)) {
             ok = false;
@@ -430,7 +434,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
         const uint32_t acc_phase = (local >> 1) & 1u;
         if (!mbar_wait<PAIR, false>(&ctl->tmem_empty[acc], acc_phase ^ 1u, &ctl->abort, p.err)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * TN;
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait<false, false>(&ctl->full[stage], phase, &ctl->abort, p.err)) {
             ok = false;
@@ -475,12 +479,12 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
       if (!ok) break;
       tc_fence_after();
       int m0, n0;
-      tile_origin(p, m_units, CL, rank, tile, m0, n0);
+      tile_origin(p, m_units, CL, rank, tile, TN, m0, n0);
       const int row0 = m0 + quarter * 32;                 // this warp's 32 rows; lane = row within them
-      const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+      const uint32_t taddr = tmem_base + acc * TN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int box = 0; box < BN / 2 / kOutCols; ++box) {
-        const int cbase = half * (BN / 2) + box * kOutCols;   // tile column of the box
+      for (int box = 0; box < TN / 2 / kOutCols; ++box) {
+        const int cbase = half * (TN / 2) + box * kOutCols;   // tile column of the box
         const int col0 = n0 + cbase;
         // the previous box's store has finished reading the staging buffer
         if (lane == 0) bulk_wait_read_all();
@@ -581,7 +585,7 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
   if (PAIR) cluster_sync();                // no copy, commit or remote arrive is left in flight to either CTA
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc<PAIR>(tmem_base);
+    tmem_dealloc<PAIR>(tmem_base, tmem_cols(TN));
   }
 }
 
@@ -622,14 +626,14 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8, bool PAIR>
+template <bool FP8, bool PAIR, int TN>
 cudaError_t launch_gemm(const CUtensorMap& map_x, const CUtensorMap& map_w, const CUtensorMap& map_y,
                         const GemmParams& p, int sms,
                         cudaStream_t stream, const char** why) {
-  auto kern = linear_bias_gelu_kernel<FP8, PAIR>;
+  auto kern = linear_bias_gelu_kernel<FP8, PAIR, TN>;
   constexpr int CL = PAIR ? 2 : 1;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes<PAIR>()));
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem_bytes<PAIR, TN>()));
   if (e != cudaSuccess) {
     *why = "could not reserve shared memory";
     return e;
@@ -637,7 +641,7 @@ cudaError_t launch_gemm(const CUtensorMap& map_x, const CUtensorMap& map_w, cons
   const int units = ((p.m_tiles + CL - 1) / CL) * p.n_tiles;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes<PAIR>();
+  cfg.dynamicSmemBytes = smem_bytes<PAIR, TN>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -679,8 +683,16 @@ cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, cons
   const bool fp8 = a.fp8 != 0;
   const int m_tiles = static_cast<int>((a.m + BM - 1) / BM);
   const bool pair = m_tiles >= 2;                        // CTA pairs on adjacent M tiles
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // A single M tile (a decode batch of at most 128 rows) with fewer 256-wide
+  // N tiles than SMs takes 128-wide N tiles: twice the CTAs stream W, which
+  // is nearly all such a launch reads.
+  const bool narrow = !pair && (a.n + BN - 1) / BN < sms;
+  const int tn = narrow ? BN_NARROW : BN;
   CUtensorMap map_x, map_w, map_y;
-  if (!make_map(&map_x, a.x, a.m, a.k, BM, fp8) || !make_map(&map_w, a.w, a.n, a.k, pair ? BN / 2 : BN, fp8) ||
+  if (!make_map(&map_x, a.x, a.m, a.k, BM, fp8) || !make_map(&map_w, a.w, a.n, a.k, pair ? BN / 2 : tn, fp8) ||
       !make_map(&map_y, a.y, a.m, a.n, 32, false)) {
     *why = "cuTensorMapEncodeTiled is unavailable or rejected the operands";
     return cudaErrorInvalidValue;
@@ -694,18 +706,17 @@ cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, cons
   p.n = static_cast<int>(a.n);
   p.k = static_cast<int>(a.k);
   p.m_tiles = m_tiles;
-  p.n_tiles = static_cast<int>((a.n + BN - 1) / BN);
+  p.n_tiles = static_cast<int>((a.n + tn - 1) / tn);
   p.act = a.act;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaError_t e;
   if (fp8)
-    e = pair ? launch_gemm<true, true>(map_x, map_w, map_y, p, sms, stream, why)
-             : launch_gemm<true, false>(map_x, map_w, map_y, p, sms, stream, why);
+    e = pair     ? launch_gemm<true, true, BN>(map_x, map_w, map_y, p, sms, stream, why)
+        : narrow ? launch_gemm<true, false, BN_NARROW>(map_x, map_w, map_y, p, sms, stream, why)
+                 : launch_gemm<true, false, BN>(map_x, map_w, map_y, p, sms, stream, why);
   else
-    e = pair ? launch_gemm<false, true>(map_x, map_w, map_y, p, sms, stream, why)
-             : launch_gemm<false, false>(map_x, map_w, map_y, p, sms, stream, why);
+    e = pair     ? launch_gemm<false, true, BN>(map_x, map_w, map_y, p, sms, stream, why)
+        : narrow ? launch_gemm<false, false, BN_NARROW>(map_x, map_w, map_y, p, sms, stream, why)
+                 : launch_gemm<false, false, BN>(map_x, map_w, map_y, p, sms, stream, why);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -42,7 +42,7 @@ def run_gpu(gbf, c, xq, wq, act, with_bias=True):
 
 @pytest.mark.parametrize("m,n,k", [(128, 256, 128), (256, 512, 512), (200, 272, 384), (1, 16, 128),
                                    (129, 256, 1024), (300, 784, 256), (1152, 4352, 256), (256, 16, 128),
-                                   (384, 48, 128)])
+                                   (384, 48, 128), (64, 4096, 512)])
 @pytest.mark.parametrize("act", [ops.ACT_GELU_TANH, 0, ops.ACT_GELU_ERF, ops.ACT_SILU])
 def test_shapes_and_activations(gbf, m, n, k, act):
     c = workloads.fp8_linear_case(m, n, k, seed=m + n + k)

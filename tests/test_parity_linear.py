@@ -31,7 +31,8 @@ def run(gbf, x_bits, w_bits, b_bits, act=1):
 
 @pytest.mark.parametrize("m,n,k", [(128, 256, 64), (256, 512, 256), (200, 256, 128), (130, 272, 192), (1, 16, 64),
                                    (384, 768, 1024), (1000, 2064, 512), (1152, 4352, 256),
-                                   (256, 16, 64), (384, 48, 128), (257, 80, 64)])
+                                   (256, 16, 64), (384, 48, 128), (257, 80, 64),
+                                   (32, 4096, 512), (100, 2320, 256)])
 def test_shapes(gbf, m, n, k):
     c = workloads.linear_gelu_case(m, n, k, seed=m + n + k)
     y = run(gbf, c["x"], c["w"], c["bias"])
