@@ -1054,12 +1054,13 @@ def main_gpu(args):
 
     # decode-shaped QKV into a paged KV cache: launch-bound, timed on its own
     # (outside the step, so the step's aggregate keeps its composition)
-    if "qwen3_qkv" in per_op:
-        line["latency_bound"]["qwen3_qkv_decode_paged"] = measure_decode_paged(gbf, flush_l2)
-    if "swiglu_ffn" in per_op:
-        line["latency_bound"]["swiglu_decode"] = measure_swiglu_decode(gbf, flush_l2)
-    if "linear_bias_gelu" in per_op:
-        line["latency_bound"]["linear_decode"] = measure_linear_decode(gbf, flush_l2)
+    if not args.no_latency_extras:
+        if "qwen3_qkv" in per_op:
+            line["latency_bound"]["qwen3_qkv_decode_paged"] = measure_decode_paged(gbf, flush_l2)
+        if "swiglu_ffn" in per_op:
+            line["latency_bound"]["swiglu_decode"] = measure_swiglu_decode(gbf, flush_l2)
+        if "linear_bias_gelu" in per_op:
+            line["latency_bound"]["linear_decode"] = measure_linear_decode(gbf, flush_l2)
 
     # end to end through the C ABI with host buffers: H2D inputs, op, D2H outputs
     if not args.no_e2e:
@@ -1470,6 +1471,8 @@ def main():
     ap.add_argument("--no-gemm", action="store_true", help="leave the GEMM row out of the step")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--no-latency-extras", action="store_true",
+                    help="skip the decode-shape latency measurements taken after the step")
     ap.add_argument("--e2e-copy-streams", type=int, default=1, help="copy streams per direction in the e2e pass")
     ap.add_argument("--only", default="", help="comma-separated subset of: " + ", ".join(OP_NAMES))
     ap.add_argument("--small", action="store_true", help="profiling-size cases (still larger than L2)")
