@@ -68,7 +68,6 @@ constexpr int BN = 256;                          // N tile (CTA pairs and most u
 constexpr int BN_NARROW = 128;                   // N tile of unpaired launches with few tiles
 constexpr int BK_BYTES = 128;                    // one 128-byte swizzle row of K per k-block
 constexpr int UMMA_K_BYTES = 32;                 // K of one MMA: 16 bf16 or 32 E4M3 values
-constexpr int A_STAGE_BYTES = BM * BK_BYTES;     // 16 KB
 // TMEM columns: two float32 accumulators of the N tile (all 512 at BN)
 constexpr int tmem_cols(int tn) { return 2 * tn; }
 constexpr int kThreads = 384;
@@ -82,14 +81,21 @@ constexpr int kOutBoxBytes = 32 * kOutCols * 2;              // 4 KB
 constexpr int kOutBytes = kEpilogueWarps * kOutBoxBytes;      // 32 KB
 
 // Shared-memory ring of one CTA: unpaired, the whole W tile per stage; paired,
-// half of it (the other half sits in the other CTA).  32 KB stages take a
-// six-deep ring, 48 KB ones (unpaired, 256-wide) three.
-template <bool PAIR, int TN>
+// half of it (the other half sits in the other CTA).  AR of the tile's 128 X
+// rows are loaded per stage: all of them, or, for a decode batch of at most
+// 32 or 64 rows, only those (the MMA still reads 128 rows from the stage's
+// start, the rest being other stages' bytes whose products fall in output
+// rows the clipped stores never write), so more stages of W are in flight.
+// 32 KB stages take a six-deep ring, 48 KB ones (unpaired, 256-wide) three,
+// the smaller decode stages as many as 192 KB holds.
+template <bool PAIR, int TN, int AR>
 struct Ring {
+  static constexpr int kKH = AR < BM ? 2 : 1;               // 128-byte K rows per stage
   static constexpr int kBRows = PAIR ? TN / 2 : TN;
-  static constexpr int kStages = A_STAGE_BYTES + kBRows * BK_BYTES <= 32768 ? 6 : 3;
-  static constexpr int kBStageBytes = kBRows * BK_BYTES;
-  static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes;
+  static constexpr int kAStageBytes = AR * BK_BYTES * kKH;
+  static constexpr int kBStageBytes = kBRows * BK_BYTES * kKH;
+  static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+  static constexpr int kStages = AR < BM ? 196608 / kStageBytes : (kStageBytes <= 32768 ? 6 : 3);
 };
 
 template <int S>
@@ -104,10 +110,10 @@ struct __align__(8) SharedCtl {
   int abort;
 };
 
-template <bool PAIR, int TN>
+template <bool PAIR, int TN, int AR>
 constexpr size_t smem_bytes() {
-  return 1024 /* alignment slack */ + Ring<PAIR, TN>::kStages * Ring<PAIR, TN>::kStageBytes + kOutBytes +
-         sizeof(SharedCtl<Ring<PAIR, TN>::kStages>);
+  using R = Ring<PAIR, TN, AR>;
+  return 1024 /* alignment slack */ + R::kStages * R::kStageBytes + kOutBytes + sizeof(SharedCtl<R::kStages>);
 }
 
 // ------------------------------------------------------------ PTX wrappers
@@ -326,11 +332,14 @@ GBF_DEVICE void tile_origin(const GemmParams& p, int m_units, int cl, int rank, 
   n0 = (n_base + idx % gs) * tn;
 }
 
-template <bool FP8, bool PAIR, int TN>
+template <bool FP8, bool PAIR, int TN, int AR>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                         const __grid_constant__ CUtensorMap map_y, const GemmParams p) {
-  using R = Ring<PAIR, TN>;
+  using R = Ring<PAIR, TN, AR>;
+  static_assert(AR == BM || !PAIR, "pairs load every X row");
+  static_assert(AR == BM || R::kStages * R::kBStageBytes >= BM * BK_BYTES - R::kAStageBytes,
+                "the MMA's reads past the last A stage stay inside the ring");
   constexpr int S = R::kStages;
   constexpr int CL = PAIR ? 2 : 1;
   constexpr int BK = FP8 ? BK_BYTES : BK_BYTES / 2;         // K elements per k-block
@@ -339,8 +348,8 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
   // the same offsets in both CTAs of a pair: the MMAs address the odd CTA's
   // operands by the even CTA's shared addresses
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* smem_a = smem;                                   // S x 16 KB
-  uint8_t* smem_b = smem + S * A_STAGE_BYTES;               // S x (32 or 16) KB
+  uint8_t* smem_a = smem;                                   // S x AR rows of 128 bytes
+  uint8_t* smem_b = smem + S * R::kAStageBytes;             // S x (32 or 16) KB
   uint8_t* smem_out = smem + S * R::kStageBytes;            // 8 x 4 KB output boxes (1 KB aligned)
   SharedCtl<S>* ctl = reinterpret_cast<SharedCtl<S>*>(smem_out + kOutBytes);
 
@@ -350,7 +359,8 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
   const bool leader = rank == 0;            // issues the MMAs (always, unpaired)
   const int m_units = (p.m_tiles + CL - 1) / CL;
   const int first = blockIdx.x / CL, stride = gridDim.x / CL;
-  const int k_blocks = p.k / BK;
+  constexpr int KH = R::kKH;
+  const int k_blocks = (p.k + BK * KH - 1) / (BK * KH);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -404,13 +414,19 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
             break;
           }
           if (leader) mbar_arrive_expect_tx(&ctl->full[stage], CL * R::kStageBytes);
-          if (PAIR) {
-            const uint32_t bar = map_cluster(smem_u32(&ctl->full[stage]), 0);
-            tma_load_2d_pair(smem_a + stage * A_STAGE_BYTES, &map_x, bar, kb * BK, m0);
-            tma_load_2d_pair(smem_b + stage * R::kBStageBytes, &map_w, bar, kb * BK, n0 + rank * R::kBRows);
-          } else {
-            tma_load_2d(smem_a + stage * A_STAGE_BYTES, &map_x, &ctl->full[stage], kb * BK, m0);
-            tma_load_2d(smem_b + stage * R::kBStageBytes, &map_w, &ctl->full[stage], kb * BK, n0);
+#pragma unroll
+          for (int h = 0; h < KH; ++h) {        // KH consecutive 128-byte K rows (beyond K: zero fill)
+            const int kc = (kb * KH + h) * BK;
+            uint8_t* da = smem_a + stage * R::kAStageBytes + h * AR * BK_BYTES;
+            uint8_t* db = smem_b + stage * R::kBStageBytes + h * R::kBRows * BK_BYTES;
+            if (PAIR) {
+              const uint32_t bar = map_cluster(smem_u32(&ctl->full[stage]), 0);
+              tma_load_2d_pair(da, &map_x, bar, kc, m0);
+              tma_load_2d_pair(db, &map_w, bar, kc, n0 + rank * R::kBRows);
+            } else {
+              tma_load_2d(da, &map_x, &ctl->full[stage], kc, m0);
+              tma_load_2d(db, &map_w, &ctl->full[stage], kc, n0);
+            }
           }
           ++issued[stage];
           if (++stage == S) {
@@ -441,15 +457,17 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem_a + stage * A_STAGE_BYTES);
+          const uint32_t a_addr = smem_u32(smem_a + stage * R::kAStageBytes);
           const uint32_t b_addr = smem_u32(smem_b + stage * R::kBStageBytes);
 #pragma unroll
-          for (int kk = 0; kk < BK_BYTES / UMMA_K_BYTES; ++kk) {
-            // advance one MMA's K (32 bytes) inside the swizzled row
-            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * UMMA_K_BYTES);
-            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * UMMA_K_BYTES);
-            tc_mma<FP8, PAIR>(d_tmem, a_desc, b_desc, kIdesc, (kb | kk) != 0);
-          }
+          for (int h = 0; h < KH; ++h)
+#pragma unroll
+            for (int kk = 0; kk < BK_BYTES / UMMA_K_BYTES; ++kk) {
+              // advance one MMA's K (32 bytes) inside the swizzled row
+              const uint64_t a_desc = smem_desc_sw128(a_addr + h * AR * BK_BYTES + kk * UMMA_K_BYTES);
+              const uint64_t b_desc = smem_desc_sw128(b_addr + h * R::kBRows * BK_BYTES + kk * UMMA_K_BYTES);
+              tc_mma<FP8, PAIR>(d_tmem, a_desc, b_desc, kIdesc, (kb | h | kk) != 0);
+            }
           tc_commit<PAIR>(&ctl->empty[stage]);   // frees the stage (in both CTAs) once these MMAs have read it
           if (++stage == S) {
             stage = 0;
@@ -626,14 +644,14 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8, bool PAIR, int TN>
+template <bool FP8, bool PAIR, int TN, int AR>
 cudaError_t launch_gemm(const CUtensorMap& map_x, const CUtensorMap& map_w, const CUtensorMap& map_y,
                         const GemmParams& p, int sms,
                         cudaStream_t stream, const char** why) {
-  auto kern = linear_bias_gelu_kernel<FP8, PAIR, TN>;
+  auto kern = linear_bias_gelu_kernel<FP8, PAIR, TN, AR>;
   constexpr int CL = PAIR ? 2 : 1;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem_bytes<PAIR, TN>()));
+                                       static_cast<int>(smem_bytes<PAIR, TN, AR>()));
   if (e != cudaSuccess) {
     *why = "could not reserve shared memory";
     return e;
@@ -641,7 +659,7 @@ cudaError_t launch_gemm(const CUtensorMap& map_x, const CUtensorMap& map_w, cons
   const int units = ((p.m_tiles + CL - 1) / CL) * p.n_tiles;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes<PAIR, TN>();
+  cfg.dynamicSmemBytes = smem_bytes<PAIR, TN, AR>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -691,8 +709,10 @@ cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, cons
   // is nearly all such a launch reads.
   const bool narrow = !pair && (a.n + BN - 1) / BN < sms;
   const int tn = narrow ? BN_NARROW : BN;
+  // X rows loaded per stage: 32 or 64 for a narrow launch of that few rows
+  const int ar = narrow && a.m <= 32 ? 32 : narrow && a.m <= 64 ? 64 : BM;
   CUtensorMap map_x, map_w, map_y;
-  if (!make_map(&map_x, a.x, a.m, a.k, BM, fp8) || !make_map(&map_w, a.w, a.n, a.k, pair ? BN / 2 : tn, fp8) ||
+  if (!make_map(&map_x, a.x, a.m, a.k, ar, fp8) || !make_map(&map_w, a.w, a.n, a.k, pair ? BN / 2 : tn, fp8) ||
       !make_map(&map_y, a.y, a.m, a.n, 32, false)) {
     *why = "cuTensorMapEncodeTiled is unavailable or rejected the operands";
     return cudaErrorInvalidValue;
@@ -710,13 +730,17 @@ cudaError_t launch_linear_bias_gelu(const GemmArgs& a, cudaStream_t stream, cons
   p.act = a.act;
   cudaError_t e;
   if (fp8)
-    e = pair     ? launch_gemm<true, true, BN>(map_x, map_w, map_y, p, sms, stream, why)
-        : narrow ? launch_gemm<true, false, BN_NARROW>(map_x, map_w, map_y, p, sms, stream, why)
-                 : launch_gemm<true, false, BN>(map_x, map_w, map_y, p, sms, stream, why);
+    e = pair        ? launch_gemm<true, true, BN, BM>(map_x, map_w, map_y, p, sms, stream, why)
+        : ar == 32  ? launch_gemm<true, false, BN_NARROW, 32>(map_x, map_w, map_y, p, sms, stream, why)
+        : ar == 64  ? launch_gemm<true, false, BN_NARROW, 64>(map_x, map_w, map_y, p, sms, stream, why)
+        : narrow    ? launch_gemm<true, false, BN_NARROW, BM>(map_x, map_w, map_y, p, sms, stream, why)
+                    : launch_gemm<true, false, BN, BM>(map_x, map_w, map_y, p, sms, stream, why);
   else
-    e = pair     ? launch_gemm<false, true, BN>(map_x, map_w, map_y, p, sms, stream, why)
-        : narrow ? launch_gemm<false, false, BN_NARROW>(map_x, map_w, map_y, p, sms, stream, why)
-                 : launch_gemm<false, false, BN>(map_x, map_w, map_y, p, sms, stream, why);
+    e = pair        ? launch_gemm<false, true, BN, BM>(map_x, map_w, map_y, p, sms, stream, why)
+        : ar == 32  ? launch_gemm<false, false, BN_NARROW, 32>(map_x, map_w, map_y, p, sms, stream, why)
+        : ar == 64  ? launch_gemm<false, false, BN_NARROW, 64>(map_x, map_w, map_y, p, sms, stream, why)
+        : narrow    ? launch_gemm<false, false, BN_NARROW, BM>(map_x, map_w, map_y, p, sms, stream, why)
+                    : launch_gemm<false, false, BN, BM>(map_x, map_w, map_y, p, sms, stream, why);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
