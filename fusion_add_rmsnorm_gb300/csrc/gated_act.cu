@@ -14,10 +14,11 @@
 // arithmetic; float32 math, one bf16 rounding, 16-byte stores.  A launch
 // with fewer (row, tile) pairs than SMs (a decode batch) cuts its rows into
 // more, smaller tiles (down to 64 vectors, at most one tile per SM), so the
-// work spreads over the SMs and a thread's critical path is about one vector.  SiLU uses
-// the fast exponential and division intrinsics and the tanh GELU the
-// hardware tanh approximation (both well inside a bf16 rounding); the erf
-// GELU calls erff.  Launched with programmatic dependent launch.
+// work spreads over the SMs and a thread's critical path is about one
+// vector.  SiLU uses the fast exponential and division intrinsics and the
+// tanh GELU the hardware tanh approximation (both well inside a bf16
+// rounding); the erf GELU calls erff.  Launched with programmatic dependent
+// launch.
 #include <map>
 #include <mutex>
 

@@ -82,12 +82,13 @@ constexpr int kOutBytes = kEpilogueWarps * kOutBoxBytes;      // 32 KB
 
 // Shared-memory ring of one CTA: unpaired, the whole W tile per stage; paired,
 // half of it (the other half sits in the other CTA).  AR of the tile's 128 X
-// rows are loaded per stage: all of them, or, for a decode batch of at most
-// 32 or 64 rows, only those (the MMA still reads 128 rows from the stage's
-// start, the rest being other stages' bytes whose products fall in output
-// rows the clipped stores never write), so more stages of W are in flight.
-// 32 KB stages take a six-deep ring, 48 KB ones (unpaired, 256-wide) three,
-// the smaller decode stages as many as 192 KB holds.
+// rows are loaded per 128-byte K row: all of them, or, for a decode batch of
+// at most 32 or 64 rows, only those (the MMA still reads 128 rows from each
+// K row's start, the rest being other bytes of the ring whose products land
+// in output rows the clipped stores never write); decode stages then hold
+// KH = 2 consecutive K rows, so each W row is read in 256-byte runs and more
+// of W is in flight.  32 KB stages take a six-deep ring, 48 KB ones
+// (unpaired, 256-wide) three, decode stages as many as 192 KB holds.
 template <bool PAIR, int TN, int AR>
 struct Ring {
   static constexpr int kKH = AR < BM ? 2 : 1;               // 128-byte K rows per stage
@@ -338,8 +339,8 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
                         const __grid_constant__ CUtensorMap map_y, const GemmParams p) {
   using R = Ring<PAIR, TN, AR>;
   static_assert(AR == BM || !PAIR, "pairs load every X row");
-  static_assert(AR == BM || R::kStages * R::kBStageBytes >= BM * BK_BYTES - R::kAStageBytes,
-                "the MMA's reads past the last A stage stay inside the ring");
+  static_assert(AR == BM || R::kStages * R::kBStageBytes >= (BM - AR) * BK_BYTES,
+                "the MMA's reads past the last A rows stay inside the ring");
   constexpr int S = R::kStages;
   constexpr int CL = PAIR ? 2 : 1;
   constexpr int BK = FP8 ? BK_BYTES : BK_BYTES / 2;         // K elements per k-block
@@ -348,8 +349,8 @@ linear_bias_gelu_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_
   // the same offsets in both CTAs of a pair: the MMAs address the odd CTA's
   // operands by the even CTA's shared addresses
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* smem_a = smem;                                   // S x AR rows of 128 bytes
-  uint8_t* smem_b = smem + S * R::kAStageBytes;             // S x (32 or 16) KB
+  uint8_t* smem_a = smem;                                   // S x KH x AR rows of 128 bytes
+  uint8_t* smem_b = smem + S * R::kAStageBytes;             // S x KH x kBRows rows of 128 bytes
   uint8_t* smem_out = smem + S * R::kStageBytes;            // 8 x 4 KB output boxes (1 KB aligned)
   SharedCtl<S>* ctl = reinterpret_cast<SharedCtl<S>*>(smem_out + kOutBytes);
 
