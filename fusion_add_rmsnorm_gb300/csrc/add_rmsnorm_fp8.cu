@@ -383,26 +383,27 @@ AddRmsNormPlan plan_add_rmsnorm(int64_t rows, int64_t hidden, int mode) {
     while (nv < 2 && nvec > 64 * nv) nv *= 2;
     p.fac = nv == 1 ? kFacReg : kFacPack;
   } else {
-    // Vectors per thread: 2 for streaming launches (half the per-row
-    // reduction and loop work per element), and for rows of 2048 values or
-    // more in smaller ones (half the warps a row reduces over); 1 for
-    // AdaRMSNorm rows in launches of one to four rows per SM, where the
-    // shared-memory copy of two-vector factors costs more than it saves
-    // ([256, 4096]: 4.35 us with one vector against 4.6-4.9 with two;
-    // [2048, 4096]: 15.3 against 12.3-12.6); more when a row would need more
-    // than the block's threads.  Factors: float32 in registers where they fit
-    // (one vector, or two without AdaRMSNorm); in a launch of at most one row
-    // per SM, packed in registers up to four vectors (no shared-memory copy
-    // and barrier ahead of the row; registers are not what bounds such a
-    // launch); else in shared memory.  Measured per call in 100-call CUDA
-    // graphs: [32, 8192] gated AdaRMSNorm 2.32 us against 3.22 with shared
-    // factors, [128, 4096] weighted 2.24 against 2.75-2.81 with one vector.
-    const bool latency = rows <= sm_count();
-    const int target =
-        large || (nvec >= 256 && (mode != kNormAda || latency || rows > 4LL * sm_count())) ? 2 : 1;
+    // Vectors per thread: 2 for streaming launches and for rows of 2048 values
+    // or more in smaller ones (half the per-row reduction and loop work per
+    // element, half the warps a row reduces over); more when a row would
+    // need more than the block's threads.  Factors: float32 in registers where
+    // they fit (one vector, or two without AdaRMSNorm); packed in registers
+    // for AdaRMSNorm at two vectors up to 16 rows per SM and for four vectors
+    // up to 4 rows per SM (no shared-memory copy and barrier ahead of the
+    // first row; the lower occupancy of the larger register set costs less
+    // there); else in shared memory.  Measured per call: gated AdaRMSNorm
+    // [32, 8192] 2.32 us against 3.22 with shared factors (100-call CUDA
+    // graph), [256, 4096] 3.6 against 4.4 with one vector, [2048, 4096] 11.6
+    // against 12.6 with shared factors; [1216, 8192] weighted 13.1 with
+    // shared factors against 13.9 with packed ones (hence the lower limit at
+    // four vectors); [128, 4096] weighted 2.24 against 2.75-2.81 with one
+    // vector.
+    const int64_t sms = sm_count();
+    const int target = large || nvec >= 256 ? 2 : 1;
     while (nv < 8 && ((nv < target && nvec >= 16 * nv) || nvec > static_cast<int64_t>(nv) * max_block(nv)))
       nv *= 2;
-    p.fac = nv == 1 || (nv == 2 && mode != kNormAda) ? kFacReg : (latency && nv <= 4 ? kFacPack : kFacSmem);
+    const bool pack = (nv == 2 && rows <= 16 * sms) || (nv == 4 && rows <= 4 * sms);
+    p.fac = nv == 1 || (nv == 2 && mode != kNormAda) ? kFacReg : (pack ? kFacPack : kFacSmem);
   }
   int tpr = 8;
   while (static_cast<int64_t>(tpr) * nv < nvec) tpr *= 2;
