@@ -3,6 +3,8 @@ DRAM-traffic record changes with the code and not with comments or layout."""
 import importlib.util
 import os
 
+import numpy as np
+
 from conftest import ROOT
 
 
@@ -84,3 +86,24 @@ def test_byte_model_fused_never_exceeds_unfused():
                 assert fused < b.bytes_unfused_add_rmsnorm(rows, hidden, mode, gated), (rows, hidden, mode, gated)
     for norm in (0, 1, 2):
         assert b.bytes_qkv(64, 8, 2, 128) < b.bytes_unfused_qkv(64, 8, 2, 128, norm)
+
+
+def test_decode_paged_case_is_a_slot_mapping_into_distinct_blocks():
+    """The decode workload the bench times on the paged cache: one token per
+    sequence, each in its own 16-row block, at the row of its position."""
+    import workloads
+    c = workloads.qkv_decode_paged_case()
+    pos, slots = c["pos"].astype(np.int64), c["slots"].astype(np.int64)
+    assert c["qkv"].shape == (32, (32 + 2 * 8) * 128) and c["cache_rows"] == 16384
+    assert pos.min() >= 0 and pos.max() < 4096
+    assert slots.min() >= 0 and slots.max() < c["cache_rows"]
+    assert np.array_equal(slots % 16, pos % 16)
+    assert len(np.unique(slots // 16)) == len(slots)
+
+
+def test_latency_extras_flag_parses():
+    """`--no-latency-extras` (the launch-list capture's flag) is a bench option."""
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--help"], capture_output=True, text=True)
+    assert out.returncode == 0 and "--no-latency-extras" in out.stdout
